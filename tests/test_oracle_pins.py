@@ -1,0 +1,387 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each test checks the oracle against a value the pages print (fixtures under
+tests/golden/), a closed form, a library routine the oracle does not use for
+that step, or brute force on tiny inputs.  A plausible slip in the oracle (a
+dropped term, a wrong sign, an off-by-one in a length rule, a transposed
+operand) fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import tg_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_rules.json")
+with open(GOLDEN) as f:
+    RULES = json.load(f)
+
+F = O.FILTER
+
+
+def P(**kw):
+    kw.setdefault("vocab", 16)
+    return O.Params(**kw)
+
+
+# --------------------------------------------------------------------------
+# values printed on the pages
+# --------------------------------------------------------------------------
+def test_chunk_plan_worked_example():
+    for n, plan in RULES["chunk_plan"]["cases"]:
+        assert O.chunk_plan(n) == plan
+
+
+def test_chunk_plan_properties():
+    # powers of two, strictly decreasing, summing to n; empty for 0
+    assert O.chunk_plan(0) == []
+    for n in range(1, 3000):
+        plan = O.chunk_plan(n)
+        assert sum(plan) == n
+        assert all(c & (c - 1) == 0 for c in plan)
+        assert all(a > b for a, b in zip(plan, plan[1:]))
+
+
+def test_candidate_heuristic_rules():
+    assert O.INITIAL_NUM_CANDIDATES == RULES["initial_num_candidates"]["K0"]
+    for K, n, K2 in RULES["candidate_heuristic"]["cases"]:
+        assert O.next_num_candidates(K, n, 64) == K2
+    # bounds
+    assert O.next_num_candidates(1, 0, 16) == 1
+    assert O.next_num_candidates(16, 16, 16) == 16
+
+
+def test_verify_prefix_rules():
+    for c in RULES["verify_prefix"]["cases"]:
+        K = len(c["cand"])
+        assert O.matched_prefix(c["next"], c["cand"], K) == c["n"]
+        # the same through verify(), with one-hot target logits forcing argmax
+        V = 10
+        tl = np.zeros((1, K + 1, V), np.float32)
+        for j, t in enumerate(c["next"]):
+            tl[0, j, t] = 5.0
+        m, nxt, _ = O.verify(tl, np.array([c["cand"]]), K, P(vocab=V))
+        assert m[0] == c["n"]
+        assert list(nxt[0]) == c["kept"][:K + 1]
+
+
+# --------------------------------------------------------------------------
+# the "Lengths" rules, one case on each side of every boundary
+# --------------------------------------------------------------------------
+EOS = 2
+
+
+def _row(L, P_, V=16):
+    h = [(7 + 3 * i) % V for i in range(L)]
+    return h, P_
+
+
+def _eos_banned(L, Plen, **kw):
+    p = P(eos_token_ids=[EOS], **kw)
+    x = np.linspace(-1, 1, p.vocab).astype(np.float32)
+    h, _ = _row(L, Plen)
+    s, banned, _ = O.process_row(x, h, Plen, p)
+    return bool(banned[EOS])
+
+
+def test_min_length_strict():
+    assert _eos_banned(L=9, Plen=5, min_length=10)
+    assert not _eos_banned(L=10, Plen=5, min_length=10)
+
+
+def test_min_new_tokens_replaces_min_length():
+    # L < min_length but new >= min_new_tokens: NOT removed when both are set
+    assert not _eos_banned(L=12, Plen=10, min_length=50, min_new_tokens=1)
+    assert _eos_banned(L=10, Plen=10, min_length=5, min_new_tokens=1)
+    assert _eos_banned(L=14, Plen=10, min_new_tokens=5)
+    assert not _eos_banned(L=15, Plen=10, min_new_tokens=5)
+
+
+def _scores(L, Plen, **kw):
+    p = P(**kw)
+    x = np.linspace(-1, 1, p.vocab).astype(np.float32)
+    h, _ = _row(L, Plen)
+    return O.process_row(x, h, Plen, p)[0]
+
+
+def test_forced_eos_only_at_max_length_minus_one():
+    kw = dict(forced_eos_token_ids=[EOS], max_new_tokens=5)
+    for L in (6, 8):
+        s = _scores(L, 3, **kw)
+        assert np.count_nonzero(s == F) == 0
+    s = _scores(7, 3, **kw)          # 3 + 5 - 1
+    assert s[EOS] == 0.0 and np.count_nonzero(s == F) == s.size - 1
+
+
+def test_forced_bos_only_for_one_token():
+    kw = dict(forced_bos_token_id=5)
+    s = _scores(1, 1, **kw)
+    assert s[5] == 0.0 and np.count_nonzero(s == F) == s.size - 1
+    # decoder-only prompt of more than one token: no forced token
+    s = _scores(3, 3, **kw)
+    assert np.count_nonzero(s == F) == 0
+    s = _scores(2, 1, **kw)
+    assert np.count_nonzero(s == F) == 0
+
+
+def test_begin_suppress_index_shift():
+    kw = dict(begin_suppress_tokens=[4])
+    assert _scores(4, 4, **kw)[4] == F          # first new token
+    assert _scores(5, 4, **kw)[4] != F
+    # a one-token prompt with a forced bos: removed at the SECOND new token
+    kw2 = dict(begin_suppress_tokens=[4], forced_bos_token_id=9)
+    assert _scores(2, 1, **kw2)[4] == F
+    assert _scores(3, 1, **kw2)[4] != F
+    # without forced bos a one-token prompt suppresses at L == 1
+    assert _scores(1, 1, begin_suppress_tokens=[4])[4] == F
+
+
+def test_processor_order_suppress_after_forced_eos():
+    # suppress_tokens comes after forced_eos: a suppressed eos stays removed,
+    # leaving an all-removed row whose argmax is index 0
+    p = P(forced_eos_token_ids=[EOS], max_new_tokens=2, suppress_tokens=[EOS])
+    x = np.linspace(-1, 1, 16).astype(np.float32)
+    s, _, _ = O.process_row(x, [1, 2], 1, p)
+    assert np.all(s == F)
+    assert O.select_row(x, [1, 2], 1, p, 0.0)[0] == 0
+
+
+def test_forced_eos_overrides_min_length_removal():
+    p = P(eos_token_ids=[EOS], min_length=100, forced_eos_token_ids=[EOS], max_new_tokens=2)
+    x = np.linspace(-1, 1, 16).astype(np.float32)
+    s, _, _ = O.process_row(x, [1, 2], 1, p)
+    assert s[EOS] == 0.0
+
+
+# --------------------------------------------------------------------------
+# repetition penalty: closed form
+# --------------------------------------------------------------------------
+def test_repetition_penalty_closed_form():
+    p = P(vocab=5, repetition_penalty=2.0)
+    x = np.array([1.0, -1.0, 0.0, 4.0, -3.0], np.float32)
+    s, _, _ = O.process_row(x, [0, 1, 1, 2, 0], 5, p)
+    assert list(s) == [0.5, -2.0, 0.0, 4.0, -3.0]
+
+
+def test_repetition_penalty_fp32_rounding():
+    # x / 1.1 rounds once in binary32, not in binary64
+    p = P(vocab=2, repetition_penalty=1.1)
+    x = np.array([1.0, -1.0], np.float32)
+    s, _, _ = O.process_row(x, [0, 1], 2, p)
+    assert s[0] == np.float32(np.float32(1.0) / np.float32(1.1))
+    assert s[1] == np.float32(np.float32(-1.0) * np.float32(1.1))
+
+
+def test_out_of_range_history_ids_skipped():
+    p = P(vocab=4, repetition_penalty=2.0)
+    x = np.array([1.0, 2.0, 3.0, 4.0], np.float32)
+    s, _, info = O.process_row(x, [-1, 4, 1, 99], 4, p)
+    assert list(s) == [1.0, 1.0, 3.0, 4.0]
+    assert info.skipped_ids == 3
+
+
+def test_filter_clamp():
+    p = P(vocab=2, repetition_penalty=4.0, mode="sample", temperature=0.5)
+    x = np.array([-3e38, 1.0], np.float32)
+    s, _, _ = O.process_row(x, [0], 1, p)
+    assert s[0] == F
+    assert O.apply_temperature(np.array([F, 1.0], np.float32), p)[0] == F
+
+
+# --------------------------------------------------------------------------
+# no_repeat_ngram_size: brute force vs an independent dictionary enumeration
+# --------------------------------------------------------------------------
+def _ngram_dict_bans(h, n):
+    """Map every (n-1)-token prefix of a complete n-gram to its next tokens,
+    then look up the row's current (n-1)-token suffix."""
+    if len(h) + 1 < n:
+        return set()
+    table = {}
+    for g in zip(*[h[i:] for i in range(n)]):
+        table.setdefault(tuple(g[:-1]), set()).add(g[-1])
+    key = tuple(h[len(h) - n + 1:]) if n > 1 else ()
+    return table.get(key, set())
+
+
+def test_ngram_hand_cases():
+    assert sorted(O.ngram_banned_tokens([1, 2, 3, 1, 2], 3)) == [3]
+    assert sorted(set(O.ngram_banned_tokens([5, 6, 5], 2))) == [6]
+    assert sorted(set(O.ngram_banned_tokens([4, 4, 7], 1))) == [4, 7]
+    assert O.ngram_banned_tokens([1, 2], 4) == []
+    # L + 1 == n: only the (n-1)-suffix exists, no complete n-gram yet
+    assert O.ngram_banned_tokens([1, 2, 3], 4) == []
+    assert sorted(O.ngram_banned_tokens([1, 2, 3, 9, 1, 2, 3], 4)) == [9]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_ngram_matches_dictionary_enumeration(n):
+    rng = np.random.default_rng(7 + n)
+    for trial in range(300):
+        L = int(rng.integers(0, 40))
+        h = [int(t) for t in rng.integers(0, 4, size=L)]
+        assert set(O.ngram_banned_tokens(h, n)) == _ngram_dict_bans(h, n), (h, n)
+
+
+# --------------------------------------------------------------------------
+# a0 upcast: against torch's own bfloat16 conversion
+# --------------------------------------------------------------------------
+def test_bf16_upcast_matches_torch():
+    torch = pytest.importorskip("torch")
+    bits = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    ours = O.bf16_bits_to_f32(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    finite = np.isfinite(ref)
+    assert np.array_equal(ours[finite].view(np.uint32), ref[finite].view(np.uint32))
+    assert O.bf16_bits_to_f32(np.array([0x3F80, 0xC000], np.uint16)).tolist() == [1.0, -2.0]
+
+
+# --------------------------------------------------------------------------
+# a11 top_k: numpy.partition
+# --------------------------------------------------------------------------
+def test_top_k_threshold_matches_partition():
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        V = int(rng.integers(2, 300))
+        s = rng.integers(-5, 5, size=V).astype(np.float32)  # many ties
+        k = int(rng.integers(1, V))
+        tau = O.top_k_threshold(s, k)
+        assert tau == np.partition(s, V - k)[V - k]
+        kept = s >= tau
+        assert kept.sum() >= k
+    assert O.top_k_threshold(np.ones(5, np.float32), 0) is None
+    assert O.top_k_threshold(np.ones(5, np.float32), 5) is None
+
+
+# --------------------------------------------------------------------------
+# a12 top_p: exact rational arithmetic with the ascending-cumsum removal rule
+# --------------------------------------------------------------------------
+def _topp_kept_ascending_exact(s, p):
+    """Kept set by the "remove while the ascending cumulative mass <= 1 - p"
+    rule, evaluated exactly on the fp64 exp weights, ties ordered so that the
+    higher index is removed first."""
+    V = len(s)
+    m = max(float(v) for v in s)
+    w = [Fraction(math.exp(float(v) - m)) for v in s]
+    Z = sum(w)
+    asc = sorted(range(V), key=lambda i: (float(s[i]), -i))
+    cum = Fraction(0)
+    kept = set(range(V))
+    thr = 1 - Fraction(p)
+    for pos, i in enumerate(asc):
+        cum += w[i] / Z
+        if cum <= thr and pos < V - 1:
+            kept.discard(i)
+    # exact distance of the decisive sums from the threshold (for skipping
+    # cases too close to call in fp64)
+    return kept
+
+
+def test_top_p_matches_exact_ascending_rule():
+    rng = np.random.default_rng(11)
+    checked = 0
+    for trial in range(3000):
+        V = int(rng.integers(1, 9))
+        s = (rng.integers(-6, 6, size=V) * 0.5).astype(np.float32)
+        p = float(rng.choice([0.3, 0.5, 0.7, 0.9, 0.95]))
+        params = P(vocab=V, mode="sample", top_p=p)
+        order, n_kept, probs, _, info = O.sample_distribution(s, params)
+        if info.topp_boundary:
+            continue
+        assert set(order[:n_kept].tolist()) == _topp_kept_ascending_exact(s, p), (s, p)
+        checked += 1
+    assert checked > 2000
+
+
+# --------------------------------------------------------------------------
+# a13 greedy: D3 lowest index among maxima
+# --------------------------------------------------------------------------
+def test_greedy_lowest_index_tie_break():
+    p = P(vocab=4)
+    assert O.select_row(np.array([1, 3, 3, 2], np.float32), [0], 1, p, 0)[0] == 1
+    assert O.select_row(np.array([-0.0, 0.0, -1, -2], np.float32), [3], 1, p, 0)[0] == 0
+    assert O.select_row(np.array([0.0, -0.0, -1, -2], np.float32), [3], 1, p, 0)[0] == 0
+
+
+def test_padding_row():
+    p = P(vocab=4)
+    assert O.select_row(np.ones(4, np.float32), [], 0, p, 0.3)[0] == -1
+
+
+# --------------------------------------------------------------------------
+# a13 sampling: inverse CDF on the sorted CDF, and a chi-square check
+# --------------------------------------------------------------------------
+def test_draw_is_searchsorted_on_sorted_cdf():
+    rng = np.random.default_rng(5)
+    for trial in range(500):
+        V = int(rng.integers(1, 50))
+        s = rng.normal(0, 2, V).astype(np.float32)
+        u = float(rng.random())
+        params = P(vocab=V, mode="sample")
+        tok, info = O.select_row(s, [0], 1, params, u)
+        # independent: sort by -s with a stable sort, cumulative fp64 softmax
+        idx = np.argsort(-s.astype(np.float64), kind="stable")
+        e = np.exp(s.astype(np.float64)[idx] - s.max())
+        cdf = np.cumsum(e) / e.sum()
+        pos = min(int(np.searchsorted(cdf, u, side="right")), V - 1)
+        if not info.u_boundary:
+            assert tok == idx[pos]
+
+
+def test_sampling_frequencies_chi_square():
+    s = np.array([0.0, 1.0, -1.0, 2.0, 0.5], np.float32)
+    params = P(vocab=5, mode="sample")
+    rng = np.random.default_rng(123)
+    N = 100_000
+    us = rng.random(N)
+    counts = np.zeros(5)
+    order, n_kept, probs, _, _ = O.sample_distribution(s, params)
+    for u in us:
+        counts[O.draw(order, n_kept, probs, u)[0]] += 1
+    e = np.exp(s.astype(np.float64) - s.max())
+    expect = N * e / e.sum()
+    chi2 = float(((counts - expect) ** 2 / expect).sum())
+    assert chi2 < 18.47  # 99.9% quantile, 4 degrees of freedom
+
+
+def test_all_removed_row_is_uniform():
+    p = P(vocab=4, mode="sample")
+    s = np.full(4, F, np.float32)
+    order, n_kept, probs, _, _ = O.sample_distribution(s, p)
+    assert np.allclose(probs, 0.25)
+    tok, ub = O.draw(order, n_kept, probs, 0.6)
+    assert tok == 2 and not ub
+    tok, ub = O.draw(order, n_kept, probs, 0.5)
+    assert tok == 2 and ub
+
+
+def test_temperature_then_top_k_then_top_p_order():
+    # top_k keeps the two largest; top_p=0.5 then keeps only the first of them
+    p = P(vocab=4, mode="sample", temperature=0.5, top_k=2, top_p=0.5)
+    s = np.array([1.0, 0.9, 0.0, -1.0], np.float32)
+    st = O.apply_temperature(s, p)
+    assert list(st) == [2.0, np.float32(0.9) / np.float32(0.5), 0.0, -2.0]
+    order, n_kept, probs, _, _ = O.sample_distribution(st, p)
+    assert probs[2] == 0 and probs[3] == 0
+    assert list(order[:n_kept]) == [0]
+
+
+# --------------------------------------------------------------------------
+# identities
+# --------------------------------------------------------------------------
+def test_identity_settings_leave_scores_unchanged():
+    rng = np.random.default_rng(9)
+    x = rng.normal(0, 3, 64).astype(np.float32)
+    h = [int(t) for t in rng.integers(0, 64, 20)]
+    p = P(vocab=64, mode="sample", repetition_penalty=1.0, temperature=1.0, top_k=0, top_p=1.0)
+    s, banned, _ = O.process_row(x, h, 10, p)
+    assert np.array_equal(s, x) and not banned.any()
+    st = O.apply_temperature(s, p)
+    assert np.array_equal(st, x)
+    for k in (0, 64, 100):
+        p.top_k = k
+        _, n_kept, probs, filt, _ = O.sample_distribution(st, p)
+        assert n_kept == 64 and np.array_equal(filt, x)
