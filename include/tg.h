@@ -1,0 +1,200 @@
+/*
+ * tg.h -- C ABI of the GB300 token-selection library (libtg.so).
+ *
+ * One decode step of autoregressive generation ends with token selection:
+ * the logits processors of transformers run over each row's scores in a fixed
+ * order, then greedy argmax or a multinomial draw picks the row's next token.
+ * The order and the length rules follow "Transmuter.Generation (transmuter
+ * v2.0.0)": module intro (processor order), section "Lengths" (how a row's
+ * length counts prompt and new tokens, and when min_length, min_new_tokens,
+ * forced bos/eos and begin_suppress_tokens apply), section "Log-probabilities"
+ * (f32 scores, the smallest finite f32 as the filter value) and section
+ * "Batches" (ragged rows, empty rows give no token).  The verify step follows
+ * "Assisted Generation: a new direction toward low-latency text generation",
+ * section "Greedy decoding with assisted generation", steps 2-6.
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are CUDA device (or managed) memory of the device that
+ *    was current when the config was created; that device must be current at
+ *    every call.  The caller owns them; the library never frees or keeps
+ *    them past the call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and the call returns without waiting.  Results are ready when the
+ *    stream reaches that point.
+ *  - Argument errors are found on the host and returned before anything is
+ *    enqueued.  A failed launch returns TG_ERR_CUDA.  Bad values that only
+ *    the device sees (history ids outside [0, V), inconsistent offsets) never
+ *    fault: the kernel skips them and raises a bit in the config's status
+ *    word (tg_query_status).
+ *  - Calls that share a tg_config use its small device workspace (verify
+ *    tickets, status word); issue them in stream order (one stream, or
+ *    events between streams).  Use one config per concurrent stream.
+ *  - Scores: the filter value F is -FLT_MAX; no score goes below it.
+ */
+#ifndef TG_H_
+#define TG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is a struct CUstream_st* */
+typedef struct CUstream_st* tg_stream;
+
+typedef enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARGUMENT = -1,
+  TG_ERR_UNSUPPORTED = -2,
+  TG_ERR_CUDA = -3,
+  TG_ERR_OUT_OF_MEMORY = -4
+} tg_status;
+
+typedef enum { TG_DTYPE_F32 = 0, TG_DTYPE_BF16 = 1 } tg_dtype;
+typedef enum { TG_GREEDY = 0, TG_SAMPLE = 1 } tg_mode;
+
+/* Status-word bits (sticky until tg_clear_status). */
+#define TG_FLAG_HISTORY_ID_OUT_OF_RANGE 0x1u /* a history id was < 0 or >= V; skipped */
+#define TG_FLAG_BAD_ROW 0x2u                 /* offsets/prompt length inconsistent; row gave -1 */
+#define TG_FLAG_SLOW_PATH 0x4u               /* a row needed the multi-pass exact path */
+
+/* Largest vocabulary the kernels take. */
+#define TG_MAX_VOCAB (1 << 18)
+/* Longest list accepted for eos ids and forced eos ids. */
+#define TG_MAX_EOS 8
+
+/*
+ * Generation settings, named after transformers' generation_config fields.
+ * Host pointers; tg_config_create copies what it needs.  tg_params_init
+ * fills the "off" defaults.
+ */
+typedef struct tg_params {
+  int32_t vocab;                /* V, 1 .. TG_MAX_VOCAB */
+  tg_dtype logits_dtype;        /* element type of the logits rows */
+  tg_mode mode;                 /* greedy argmax or multinomial draw */
+  float repetition_penalty;     /* > 0; 1 = off */
+  int32_t no_repeat_ngram_size; /* >= 0; 0 = off */
+  const int32_t* bad_words_ids; /* single-token bad words, each in [0, V) */
+  int32_t n_bad_words_ids;
+  const int32_t* suppress_tokens; /* each in [0, V) */
+  int32_t n_suppress_tokens;
+  const int32_t* begin_suppress_tokens; /* each in [0, V) */
+  int32_t n_begin_suppress_tokens;
+  const int32_t* eos_token_ids; /* removed while min_length/min_new_tokens hold */
+  int32_t n_eos_token_ids;      /* 0 .. TG_MAX_EOS */
+  int32_t min_length;           /* >= 0; 0 = off */
+  int32_t min_new_tokens;       /* >= 0; 0 = off; when > 0 it replaces min_length */
+  int32_t forced_bos_token_id;  /* -1 = off, else in [0, V) */
+  const int32_t* forced_eos_token_ids; /* forced at L == prompt + max_new_tokens - 1 */
+  int32_t n_forced_eos_token_ids;      /* 0 = off .. TG_MAX_EOS */
+  int32_t max_new_tokens;       /* > 0 when forced eos ids are given */
+  float temperature;            /* > 0; 1 = off (sampling only) */
+  int32_t top_k;                /* >= 0; 0 = off (sampling only) */
+  float top_p;                  /* (0, 1]; 1 = off (sampling only) */
+  int32_t max_batch;            /* largest B a tg_verify call may pass; 0 = 4096 */
+} tg_params;
+
+/* Opaque, immutable after creation; holds the constant masks on the device. */
+typedef struct tg_config tg_config;
+
+/* Fill *p with the defaults: every processor off, greedy, f32. */
+void tg_params_init(tg_params* p, int32_t vocab);
+
+/*
+ * Validate *params and build a config on the current device: sorted
+ * constant ban lists (bad words and suppress tokens), begin-suppress list,
+ * status word and verify tickets.  Synchronous.  Errors:
+ * TG_ERR_INVALID_ARGUMENT (a field out of range), TG_ERR_UNSUPPORTED
+ * (V > TG_MAX_VOCAB), TG_ERR_OUT_OF_MEMORY, TG_ERR_CUDA.
+ */
+tg_status tg_config_create(const tg_params* params, tg_config** out);
+
+/* Free the config's device memory (synchronises the device first). */
+tg_status tg_config_destroy(tg_config* cfg);
+
+/*
+ * tg_select -- process and select one token per row.
+ *
+ *  logits        device, [B, V] row-major, cfg's dtype (f32 or bf16), rows
+ *                V elements apart.  16-byte aligned rows take the bulk-copy
+ *                path; other layouts work at lower speed.
+ *  B, V          batch rows (>= 0) and vocabulary (must equal cfg's vocab).
+ *  hist_ids      device int32, every row's history back to back: prompt
+ *                then new tokens (unpadded; may be NULL when all rows are
+ *                empty).
+ *  hist_offsets  device int64 [B+1]; row b's history is
+ *                hist_ids[hist_offsets[b] .. hist_offsets[b+1]); its length
+ *                L is the row length the processors count.
+ *  prompt_lens   device int32 [B]; P for each row, 0 <= P <= L.
+ *  cfg           from tg_config_create.
+ *  uniforms      device f32 [B], each in [0, 1): the draw of row b.  May be
+ *                NULL in greedy mode.
+ *  out_ids       device int32 [B]; the selected id, or -1 for an empty row.
+ *
+ * Steps per row (processor order of the Transmuter.Generation module intro):
+ * repetition_penalty, no_repeat_ngram_size, bad words, min_length /
+ * min_new_tokens, forced bos, forced eos, suppress_tokens,
+ * begin_suppress_tokens; then greedy argmax (lowest index among equal
+ * maxima), or temperature, top_k, top_p and an inverse-CDF draw with
+ * uniforms[b] over the kept tokens ordered by (score desc, index asc).
+ */
+tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                    const int64_t* hist_offsets, const int32_t* prompt_lens,
+                    const tg_config* cfg, const float* uniforms, int32_t* out_ids,
+                    tg_stream stream);
+
+/*
+ * tg_verify -- assisted-generation verification (Assisted Generation,
+ * "Greedy decoding with assisted generation", steps 3-5).
+ *
+ *  target_logits device, [B, K+1, V] row-major in cfg's dtype: the target
+ *                model's logits after the prefix and after each candidate.
+ *  cand_ids      device int32 [B, K]: the assistant's candidates.
+ *  K             candidates per row, >= 1.
+ *  uniforms      device f32 [B, K+1] for sampling mode (NULL for greedy).
+ *  out_match     device int32 [B]: n_b, the number of leading candidates
+ *                equal to the target's selection.
+ *  out_next      device int32 [B, K+1]: the target's tokens 0..n_b (the
+ *                matches and the first divergent, or bonus, token); -1 after.
+ *
+ * Position j selects with cfg's mode and warpers (temperature, top_k,
+ * top_p); history processors do not run per position.  B <= cfg's max_batch.
+ */
+tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids,
+                    int32_t K, const tg_config* cfg, const float* uniforms, int32_t* out_match,
+                    int32_t* out_next, tg_stream stream);
+
+/*
+ * tg_process -- diagnostic, not tuned: the scores tg_select computes.
+ * Same inputs as tg_select, plus:
+ *  out_scores   device f32 [B, V]: scores after the processors (and after
+ *               temperature in sampling mode); rows with L == 0 untouched.
+ *  out_banbits  device uint32 [B, ceil(V/32)], or NULL: bit i of row b is set
+ *               when a ban or force processor set token i to the filter value.
+ *  out_probs    device f32 [B, V], or NULL: the distribution the draw uses
+ *               (after top_k/top_p, renormalised; 0 outside the kept set);
+ *               in greedy mode the softmax of out_scores.
+ */
+tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                     const int64_t* hist_offsets, const int32_t* prompt_lens,
+                     const tg_config* cfg, float* out_scores, uint32_t* out_banbits,
+                     float* out_probs, tg_stream stream);
+
+/* Read (synchronously) the sticky status bits and the count of rows that took
+ * the multi-pass exact path since the last clear. */
+tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_rows);
+tg_status tg_clear_status(const tg_config* cfg);
+
+/* Assisted Generation, step 6: the next candidate count.  K + 2 when
+ * n_match == K (all candidates matched), else K - 1; bounded to [1, K_max]. */
+int32_t tg_next_num_candidates(int32_t K, int32_t n_match, int32_t K_max);
+
+/* A static, human-readable name of a status code. */
+const char* tg_status_string(tg_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TG_H_ */

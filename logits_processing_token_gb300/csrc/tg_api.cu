@@ -1,0 +1,324 @@
+// C ABI of libtg (declared in include/tg.h): argument checks, config
+// creation and kernel launches.  Every check that can be made on the host is
+// made here, before anything is enqueued.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/tg.h"
+#include "tg_device.cuh"
+
+struct LaunchPlan {
+  int nstage = 0;
+  int smem = 0;
+  int blocks_per_sm = 0;
+};
+
+struct tg_config {
+  tg::DevCfg dev;
+  int device = 0;
+  int nsm = 0;
+  int V = 0;
+  int dtype = 0;
+  int mode = 0;
+  int max_batch = 0;
+  int nwords = 0;
+  LaunchPlan sel, ver;
+  int proc_smem = 0;
+  void* dmem = nullptr;
+};
+
+namespace {
+
+tg_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return TG_OK;
+  if (e == cudaErrorMemoryAllocation) return TG_ERR_OUT_OF_MEMORY;
+  return TG_ERR_CUDA;
+}
+
+bool ids_in_range(const int32_t* p, int32_t n, int32_t V) {
+  if (n < 0 || (n > 0 && !p)) return false;
+  for (int32_t i = 0; i < n; ++i)
+    if (p[i] < 0 || p[i] >= V) return false;
+  return true;
+}
+
+std::vector<int> sorted_unique(std::initializer_list<std::pair<const int32_t*, int32_t>> lists) {
+  std::vector<int> v;
+  for (auto& l : lists)
+    for (int32_t i = 0; i < l.second; ++i) v.push_back(l.first[i]);
+  std::sort(v.begin(), v.end());
+  v.erase(std::unique(v.begin(), v.end()), v.end());
+  return v;
+}
+
+// Pick the TMA ring depth: two CTAs per SM when the ring can still hold three
+// stages, else one CTA per SM with a deeper ring.
+tg_status plan_select(int dtype, bool verify, int nwords, LaunchPlan* out) {
+  int dev = 0, per_sm = 0, optin = 0, reserved = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  const int base = tg::select_smem_bytes(0, nwords);
+  for (int ctas = 2; ctas >= 1; --ctas) {
+    int budget = std::min(optin, per_sm / ctas - reserved);
+    int ns = std::min(8, (budget - base) / tg::kStageBytes);
+    if (ns < (ctas == 2 ? 3 : 2)) continue;
+    int smem = tg::select_smem_bytes(ns, nwords);
+    int occ = 0;
+    e = tg::select_occupancy(dtype, verify, smem, &occ);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (occ >= ctas || (ctas == 1 && occ >= 1)) {
+      out->nstage = ns;
+      out->smem = smem;
+      out->blocks_per_sm = ctas;
+      return TG_OK;
+    }
+  }
+  return TG_ERR_UNSUPPORTED;
+}
+
+tg_status check_device(const tg_config* cfg) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
+  return dev == cfg->device ? TG_OK : TG_ERR_INVALID_ARGUMENT;
+}
+
+}  // namespace
+
+extern "C" {
+
+void tg_params_init(tg_params* p, int32_t vocab) {
+  if (!p) return;
+  std::memset(p, 0, sizeof(*p));
+  p->vocab = vocab;
+  p->logits_dtype = TG_DTYPE_F32;
+  p->mode = TG_GREEDY;
+  p->repetition_penalty = 1.0f;
+  p->forced_bos_token_id = -1;
+  p->temperature = 1.0f;
+  p->top_p = 1.0f;
+}
+
+tg_status tg_config_create(const tg_params* p, tg_config** out) {
+  if (!p || !out) return TG_ERR_INVALID_ARGUMENT;
+  *out = nullptr;
+  const int32_t V = p->vocab;
+  if (V < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (V > TG_MAX_VOCAB) return TG_ERR_UNSUPPORTED;
+  if (p->logits_dtype != TG_DTYPE_F32 && p->logits_dtype != TG_DTYPE_BF16) return TG_ERR_INVALID_ARGUMENT;
+  if (p->mode != TG_GREEDY && p->mode != TG_SAMPLE) return TG_ERR_INVALID_ARGUMENT;
+  if (!(p->repetition_penalty > 0.0f) || !std::isfinite(p->repetition_penalty)) return TG_ERR_INVALID_ARGUMENT;
+  if (p->no_repeat_ngram_size < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (!ids_in_range(p->bad_words_ids, p->n_bad_words_ids, V)) return TG_ERR_INVALID_ARGUMENT;
+  if (!ids_in_range(p->suppress_tokens, p->n_suppress_tokens, V)) return TG_ERR_INVALID_ARGUMENT;
+  if (!ids_in_range(p->begin_suppress_tokens, p->n_begin_suppress_tokens, V)) return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_eos_token_ids > TG_MAX_EOS || !ids_in_range(p->eos_token_ids, p->n_eos_token_ids, V))
+    return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_forced_eos_token_ids > TG_MAX_EOS ||
+      !ids_in_range(p->forced_eos_token_ids, p->n_forced_eos_token_ids, V))
+    return TG_ERR_INVALID_ARGUMENT;
+  if (p->min_length < 0 || p->min_new_tokens < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (p->forced_bos_token_id < -1 || p->forced_bos_token_id >= V) return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_forced_eos_token_ids > 0 && p->max_new_tokens < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (p->max_new_tokens < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (!(p->temperature > 0.0f) || !std::isfinite(p->temperature)) return TG_ERR_INVALID_ARGUMENT;
+  if (p->top_k < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return TG_ERR_INVALID_ARGUMENT;
+  if (p->max_batch < 0) return TG_ERR_INVALID_ARGUMENT;
+
+  tg_config* cfg = new (std::nothrow) tg_config();
+  if (!cfg) return TG_ERR_OUT_OF_MEMORY;
+  tg_status st = TG_OK;
+  cudaError_t e = cudaGetDevice(&cfg->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&cfg->nsm, cudaDevAttrMultiProcessorCount, cfg->device);
+  if (e != cudaSuccess) { delete cfg; return from_cuda(e); }
+
+  cfg->V = V;
+  cfg->dtype = p->logits_dtype;
+  cfg->mode = p->mode;
+  cfg->max_batch = p->max_batch ? p->max_batch : 4096;
+  cfg->nwords = (V + 31) / 32;
+
+  std::vector<int> ban = sorted_unique({{p->bad_words_ids, p->n_bad_words_ids}, {p->suppress_tokens, p->n_suppress_tokens}});
+  std::vector<int> sup = sorted_unique({{p->suppress_tokens, p->n_suppress_tokens}});
+  std::vector<int> bsup = sorted_unique({{p->begin_suppress_tokens, p->n_begin_suppress_tokens}});
+  std::vector<int> feos = sorted_unique({{p->forced_eos_token_ids, p->n_forced_eos_token_ids}});
+
+  // one allocation: [ban][sup][bsup][tickets][status u32][pad][slow_rows u64]
+  const size_t n_int = ban.size() + sup.size() + bsup.size() + static_cast<size_t>(cfg->max_batch) + 2;
+  const size_t bytes = ((n_int * 4 + 15) / 16) * 16 + 16;
+  e = cudaMalloc(&cfg->dmem, bytes);
+  if (e != cudaSuccess) { delete cfg; return from_cuda(e); }
+  std::vector<int> host(bytes / 4, 0);
+  size_t o = 0;
+  auto put = [&](const std::vector<int>& v) { size_t at = o; std::copy(v.begin(), v.end(), host.begin() + o); o += v.size(); return at; };
+  size_t o_ban = put(ban), o_sup = put(sup), o_bsup = put(bsup);
+  size_t o_tick = o; o += cfg->max_batch;
+  size_t o_status = o; o += 1;
+  size_t o_slow = ((o * 4 + 15) / 16) * 16 / 4;
+  e = cudaMemcpy(cfg->dmem, host.data(), bytes, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) { cudaFree(cfg->dmem); delete cfg; return from_cuda(e); }
+
+  int* d = static_cast<int*>(cfg->dmem);
+  tg::DevCfg& c = cfg->dev;
+  std::memset(&c, 0, sizeof(c));
+  c.V = V;
+  c.dtype = p->logits_dtype;
+  c.mode = p->mode;
+  c.rho = p->repetition_penalty;
+  c.ngram = p->no_repeat_ngram_size;
+  c.ban_sorted = d + o_ban; c.n_ban = static_cast<int>(ban.size());
+  c.sup_sorted = d + o_sup; c.n_sup = static_cast<int>(sup.size());
+  c.bsup_sorted = d + o_bsup; c.n_bsup = static_cast<int>(bsup.size());
+  c.n_eos = p->n_eos_token_ids;
+  for (int i = 0; i < c.n_eos; ++i) c.eos[i] = p->eos_token_ids[i];
+  c.min_length = p->min_length;
+  c.min_new = p->min_new_tokens;
+  c.bos = p->forced_bos_token_id;
+  c.n_feos = static_cast<int>(feos.size());
+  for (int i = 0; i < c.n_feos; ++i) c.feos[i] = feos[i];
+  c.max_new = p->max_new_tokens;
+  c.temp = p->temperature;
+  c.top_k = p->top_k;
+  c.top_p = p->top_p;
+  c.tickets = reinterpret_cast<unsigned*>(d + o_tick);
+  c.status = reinterpret_cast<unsigned*>(d + o_status);
+  c.slow_rows = reinterpret_cast<unsigned long long*>(d + o_slow);
+
+  st = plan_select(c.dtype, false, cfg->nwords, &cfg->sel);
+  if (st == TG_OK) st = plan_select(c.dtype, true, 0, &cfg->ver);
+  cfg->proc_smem = tg::process_smem_bytes(cfg->nwords);
+  if (st != TG_OK) {
+    cudaFree(cfg->dmem);
+    delete cfg;
+    return st;
+  }
+  *out = cfg;
+  return TG_OK;
+}
+
+tg_status tg_config_destroy(tg_config* cfg) {
+  if (!cfg) return TG_ERR_INVALID_ARGUMENT;
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t e2 = cudaFree(cfg->dmem);
+  delete cfg;
+  return from_cuda(e != cudaSuccess ? e : e2);
+}
+
+tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                    const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                    const float* uniforms, int32_t* out_ids, tg_stream stream) {
+  if (!cfg || B < 0 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (!logits || !hist_offsets || !prompt_lens || !out_ids) return TG_ERR_INVALID_ARGUMENT;
+  if (cfg->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  tg::SelArgs a{};
+  a.logits = logits;
+  a.nrows = B;
+  a.V = V;
+  a.hist = hist_ids;
+  a.off = hist_offsets;
+  a.plen = prompt_lens;
+  a.uniforms = uniforms;
+  a.out = out_ids;
+  a.nstage = cfg->sel.nstage;
+  a.nwords = cfg->nwords;
+  int grid = std::min<long long>(B, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm);
+  return from_cuda(tg::launch_select(cfg->dev, a, false, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids, int32_t K,
+                    const tg_config* cfg, const float* uniforms, int32_t* out_match, int32_t* out_next,
+                    tg_stream stream) {
+  if (!cfg || B < 0 || V != cfg->V || K < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (B > cfg->max_batch) return TG_ERR_INVALID_ARGUMENT;
+  if (!target_logits || !cand_ids || !out_match || !out_next) return TG_ERR_INVALID_ARGUMENT;
+  if (cfg->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
+  if (static_cast<long long>(B) * (K + 1) > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  tg::SelArgs a{};
+  a.logits = target_logits;
+  a.nrows = B * (K + 1);
+  a.V = V;
+  a.uniforms = uniforms;
+  a.out = out_next;
+  a.cand = cand_ids;
+  a.K = K;
+  a.out_match = out_match;
+  a.nstage = cfg->ver.nstage;
+  a.nwords = 0;
+  int grid = std::min<long long>(a.nrows, static_cast<long long>(cfg->ver.blocks_per_sm) * cfg->nsm);
+  return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->ver.smem, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                     const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                     float* out_scores, uint32_t* out_banbits, float* out_probs, tg_stream stream) {
+  if (!cfg || B < 0 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (!logits || !hist_offsets || !prompt_lens || !out_scores) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  tg::SelArgs a{};
+  a.logits = logits;
+  a.nrows = B;
+  a.V = V;
+  a.hist = hist_ids;
+  a.off = hist_offsets;
+  a.plen = prompt_lens;
+  a.nwords = cfg->nwords;
+  return from_cuda(tg::launch_process(cfg->dev, a, out_scores, out_banbits, out_probs, cfg->proc_smem,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_rows) {
+  if (!cfg) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  unsigned f = 0;
+  unsigned long long s = 0;
+  cudaError_t e = cudaMemcpy(&f, cfg->dev.status, sizeof(f), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&s, cfg->dev.slow_rows, sizeof(s), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (flags) *flags = f;
+  if (slow_rows) *slow_rows = s;
+  return TG_OK;
+}
+
+tg_status tg_clear_status(const tg_config* cfg) {
+  if (!cfg) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  cudaError_t e = cudaMemset(cfg->dev.status, 0, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(cfg->dev.slow_rows, 0, sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return from_cuda(e);
+}
+
+int32_t tg_next_num_candidates(int32_t K, int32_t n_match, int32_t K_max) {
+  int32_t K2 = n_match >= K ? K + 2 : K - 1;
+  if (K_max < 1) K_max = 1;
+  return K2 < 1 ? 1 : (K2 > K_max ? K_max : K2);
+}
+
+const char* tg_status_string(tg_status s) {
+  switch (s) {
+    case TG_OK: return "TG_OK";
+    case TG_ERR_INVALID_ARGUMENT: return "TG_ERR_INVALID_ARGUMENT";
+    case TG_ERR_UNSUPPORTED: return "TG_ERR_UNSUPPORTED";
+    case TG_ERR_CUDA: return "TG_ERR_CUDA";
+    case TG_ERR_OUT_OF_MEMORY: return "TG_ERR_OUT_OF_MEMORY";
+  }
+  return "TG_UNKNOWN_STATUS";
+}
+
+}  // extern "C"

@@ -1,0 +1,679 @@
+// Device-side building blocks of the token-selection kernels (sm_103a).
+//
+// Scores follow "Transmuter.Generation (transmuter v2.0.0)": f32 scores, the
+// filter value is -FLT_MAX and no score goes below it (section
+// Log-probabilities); row lengths and the conditional processors follow its
+// section "Lengths"; the processor order follows its module intro.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace tg {
+
+constexpr int kThreads = 512;               // threads per CTA of every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kStageBytes = 16384;          // one TMA bulk copy / sub-chunk of a row
+constexpr int kCandCap = 6144;              // candidate slots of the one-pass path
+constexpr int kSpecCap = 512;               // bf16 side list of patched tokens per sub-chunk
+constexpr float kFilter = -3.40282346638528859812e+38f;  // -FLT_MAX
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr int kFixShift = 44;               // fixed-point mass: weight * 2^44, weight <= 1
+constexpr double kFixScale = 17592186044416.0;  // 2^44
+constexpr unsigned long long kWaitLimitCycles = 2000000000ull;  // ~1 s bound on any wait
+
+// Status bits (mirrors tg.h).
+constexpr unsigned kFlagBadId = 0x1u;
+constexpr unsigned kFlagBadRow = 0x2u;
+constexpr unsigned kFlagSlow = 0x4u;
+constexpr unsigned kFlagTimeout = 0x8u;
+
+enum { kGreedy = 0, kSample = 1 };
+enum { kF32 = 0, kBF16 = 1 };
+
+// Everything a kernel needs to know about the settings, passed by value.
+struct DevCfg {
+  int V;
+  int dtype;
+  int mode;
+  float rho;                  // repetition penalty
+  int ngram;                  // no_repeat_ngram_size
+  const int* ban_sorted;      // bad words + suppress tokens, sorted, unique
+  int n_ban;
+  const int* sup_sorted;      // suppress tokens, sorted, unique
+  int n_sup;
+  const int* bsup_sorted;     // begin-suppress tokens, sorted, unique
+  int n_bsup;
+  int eos[8];
+  int n_eos;
+  int min_length;
+  int min_new;
+  int bos;                    // -1 = off
+  int feos[8];                // forced eos ids, sorted, unique
+  int n_feos;
+  int max_new;
+  float temp;
+  int top_k;
+  float top_p;
+  unsigned* status;
+  unsigned long long* slow_rows;
+  unsigned* tickets;
+};
+
+struct SelArgs {
+  const void* logits;
+  int nrows;             // B (select) or B*(K+1) (verify)
+  int V;
+  const int32_t* hist;
+  const int64_t* off;
+  const int32_t* plen;
+  const float* uniforms;
+  int32_t* out;          // out_ids (select) or out_next (verify)
+  const int32_t* cand;   // verify
+  int K;
+  int32_t* out_match;
+  int nstage;
+  int nwords;
+};
+
+// Launch helpers (tg_kernels.cu).
+int select_smem_bytes(int nstage, int nwords);
+int process_smem_bytes(int nwords);
+cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s);
+cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
+                           int smem, cudaStream_t s);
+cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_sm);
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+// Order-preserving map f32 -> u32 (larger float -> larger key); -0 maps to +0.
+__device__ __forceinline__ unsigned fkey(float f) {
+  unsigned u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(unsigned k) {
+  unsigned u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ float clampf(float s) { return fmaxf(s, kFilter); }
+
+__device__ __forceinline__ float bf16lo(unsigned p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16hi(unsigned p) { return __uint_as_float(p & 0xffff0000u); }
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Fast weight used only for the excluded mass: 2^(s*log2e - m*log2e).
+__device__ __forceinline__ float wfast(float s, float c) { return ex2_approx(fmaf(s, kLog2e, -c)); }
+
+// Accurate weight exp(s - m) in fixed point (x 2^44).  s - m is formed
+// exactly as hi + lo (TwoSum); exp(hi + lo) ~= exp(hi) * (1 + lo).
+__device__ __forceinline__ unsigned long long wfix(float s, float m) {
+  float a = s, b = -m;
+  float hi = __fadd_rn(a, b);
+  float bb = __fsub_rn(hi, a);
+  float lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+  float e = expf(hi);
+  float w = fmaf(e, lo, e);
+  w = fminf(fmaxf(w, 0.0f), 1.0f);
+  return __float2ull_rn(w * 17592186044416.0f);
+}
+
+// Temperature, then the clamp at the filter value.  A patched slot holding
+// -inf stays -inf (it is counted through its side-list entry instead).
+__device__ __forceinline__ float temper(float v, float T) {
+  float q = __fdiv_rn(v, T);
+  return fmaxf(q, v == -INFINITY ? -INFINITY : kFilter);
+}
+
+__device__ __forceinline__ float penalize(float x, float rho) {
+  float s = x < 0.0f ? __fmul_rn(x, rho) : __fdiv_rn(x, rho);
+  return clampf(s);
+}
+
+// Binary search in a sorted int array (global memory, small).
+__device__ __forceinline__ bool in_sorted(const int* a, int n, int t) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    int v = __ldg(a + mid);
+    if (v < t) lo = mid + 1; else hi = mid;
+  }
+  return lo < n && __ldg(a + lo) == t;
+}
+
+// ---------------------------------------------------------------------------
+// block reductions (all threads must call)
+// ---------------------------------------------------------------------------
+struct RedScratch {
+  float f[kWarps];
+  double d[kWarps];
+  unsigned u[kWarps];
+  unsigned long long q[kWarps];
+};
+
+__device__ __forceinline__ float block_max(float v, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r->f[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = r->f[0];
+  for (int i = 1; i < kWarps; ++i) m = fmaxf(m, r->f[i]);
+  return m;
+}
+__device__ __forceinline__ float block_sum_f(float v, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r->f[threadIdx.x >> 5] = v;
+  __syncthreads();
+  // pairwise over the 16 warp partials
+  float a[kWarps];
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) a[i] = r->f[i];
+#pragma unroll
+  for (int w = kWarps / 2; w; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] += a[i + w];
+  return a[0];
+}
+// Max of m and sum of e over the block in one exchange.
+__device__ __forceinline__ void block_max_sum(float& m, float& e, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    e += __shfl_xor_sync(0xffffffffu, e, o);
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) { r->f[threadIdx.x >> 5] = m; r->u[threadIdx.x >> 5] = __float_as_uint(e); }
+  __syncthreads();
+  float a[kWarps];
+  float mm = r->f[0];
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) { a[i] = __uint_as_float(r->u[i]); mm = fmaxf(mm, r->f[i]); }
+#pragma unroll
+  for (int w = kWarps / 2; w; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] += a[i + w];
+  m = mm;
+  e = a[0];
+}
+__device__ __forceinline__ double block_sum_d(double v, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r->d[threadIdx.x >> 5] = v;
+  __syncthreads();
+  double s = 0.0;
+  for (int i = 0; i < kWarps; ++i) s += r->d[i];
+  return s;
+}
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r->q[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long s = 0;
+  for (int i = 0; i < kWarps; ++i) s += r->q[i];
+  return s;
+}
+__device__ __forceinline__ unsigned block_min_u(unsigned v, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r->u[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned m = r->u[0];
+  for (int i = 1; i < kWarps; ++i) m = min(m, r->u[i]);
+  return m;
+}
+__device__ __forceinline__ unsigned block_max_u(unsigned v, RedScratch* r) {
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r->u[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned m = r->u[0];
+  for (int i = 1; i < kWarps; ++i) m = max(m, r->u[i]);
+  return m;
+}
+
+// ---------------------------------------------------------------------------
+// Row metadata: the "Lengths" rules evaluated once per row
+// ---------------------------------------------------------------------------
+struct RowMeta {
+  long long h0;     // first history id
+  int L, P;
+  bool bad;         // inconsistent offsets / prompt length
+  bool eos_off;     // a5: eos ids removed
+  bool forced;      // a6 or a7 active
+  bool forced_eos;  // a7 active (it runs after a6 and overrides it)
+  bool bsup;        // a9: begin-suppress active
+};
+
+// Rows must form a CSR over hist_ids: 0 <= off[b] <= off[b+1] <= off[B].  A
+// row outside that, or with a prompt longer than the row, is flagged bad.
+__device__ __forceinline__ RowMeta row_meta(const DevCfg& c, const int32_t* hist, const int64_t* off,
+                                            const int32_t* plen, int b, int B) {
+  RowMeta r;
+  long long o0 = off[b], o1 = off[b + 1], oend = off[B];
+  int P = plen[b];
+  r.h0 = o0;
+  long long L = o1 - o0;
+  r.bad = (o0 < 0) || (L < 0) || (o1 > oend) || (L > 0x7fffffffLL) || (P < 0) || (P > L) ||
+          (hist == nullptr && L > 0);
+  r.L = r.bad ? 0 : static_cast<int>(L);
+  r.P = r.bad ? 0 : P;
+  int Li = r.L, new_tokens = r.L - r.P;
+  if (c.min_new > 0) r.eos_off = new_tokens < c.min_new;
+  else r.eos_off = c.min_length > 0 && Li < c.min_length;
+  bool fb = c.bos >= 0 && Li == 1;
+  r.forced_eos = c.n_feos > 0 && Li == r.P + c.max_new - 1;
+  r.forced = fb || r.forced_eos;
+  int bidx = (c.bos >= 0 && r.P == 1) ? r.P + 1 : r.P;
+  r.bsup = c.n_bsup > 0 && Li == bidx;
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Per-row bitmaps in shared memory: H = history ids (penalised, only when
+// rho != 1), N = banned (n-gram, bad words, eos under min length, suppress,
+// begin-suppress).  nwords = ceil(V/32).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_bit(unsigned* bm, int t) { atomicOr(bm + (t >> 5), 1u << (t & 31)); }
+__device__ __forceinline__ bool get_bit(const unsigned* bm, int t) { return (bm[t >> 5] >> (t & 31)) & 1u; }
+
+__device__ __forceinline__ void build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
+                                  unsigned* H, unsigned* N, int nwords) {
+  const int tid = threadIdx.x;
+  for (int w = tid; w < nwords; w += kThreads) { H[w] = 0u; N[w] = 0u; }
+  __syncthreads();
+  const int V = c.V;
+  const int32_t* h = hist + r.h0;
+  const int L = r.L;
+  bool bad_id = false;
+  if (c.rho != 1.0f) {
+    for (int i = tid; i < L; i += kThreads) {
+      int t = __ldg(h + i);
+      if (t >= 0 && t < V) set_bit(H, t); else bad_id = true;
+    }
+  } else {
+    for (int i = tid; i < L; i += kThreads) {
+      int t = __ldg(h + i);
+      if (t < 0 || t >= V) bad_id = true;
+    }
+  }
+  // no_repeat_ngram_size: start j bans h[j+n-1] when h[j..j+n-2] equals the
+  // row's last n-1 tokens.
+  const int n = c.ngram;
+  if (n > 0 && L + 1 >= n) {
+    const int last = L - n;  // last start of a complete n-gram
+    const int s0 = L - n + 1;
+    const int first_tok = n > 1 ? __ldg(h + s0) : 0;
+    for (int j = tid; j <= last; j += kThreads) {
+      bool eq = true;
+      if (n > 1) {
+        eq = __ldg(h + j) == first_tok;
+        for (int q = 1; eq && q < n - 1; ++q) eq = __ldg(h + j + q) == __ldg(h + s0 + q);
+      }
+      if (eq) {
+        int t = __ldg(h + j + n - 1);
+        if (t >= 0 && t < V) set_bit(N, t);
+      }
+    }
+  }
+  for (int i = tid; i < c.n_ban; i += kThreads) set_bit(N, __ldg(c.ban_sorted + i));
+  if (r.eos_off && tid < c.n_eos) set_bit(N, c.eos[tid]);
+  if (r.bsup)
+    for (int i = tid; i < c.n_bsup; i += kThreads) set_bit(N, __ldg(c.bsup_sorted + i));
+  if (bad_id) atomicOr(c.status, kFlagBadId);
+  __syncthreads();
+}
+
+// Processed score of one token from its raw value and the row bitmaps
+// (a2-a9 for a row that is not forced), then temperature when sampling.
+__device__ __forceinline__ float process_elem(const DevCfg& c, const unsigned* H, const unsigned* N,
+                                              float x, int i, bool sample) {
+  float s = x;
+  if (get_bit(N, i)) s = kFilter;
+  else if (get_bit(H, i)) s = penalize(x, c.rho);
+  if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// Forced rows (a6/a7 active): every token is the filter value except the
+// forced ids, which score 0, unless suppress_tokens or begin_suppress_tokens
+// remove them again (a8, a9 run after the forcing).  The zero-scored ids are
+// returned sorted and unique in zs[0..nz).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int forced_zeros(const DevCfg& c, const RowMeta& r, int* zs) {
+  int cand[8];
+  int nc = 0;
+  if (r.forced_eos) {
+    for (int i = 0; i < c.n_feos; ++i) cand[nc++] = c.feos[i];
+  } else {
+    cand[nc++] = c.bos;
+  }
+  int nz = 0;
+  for (int i = 0; i < nc; ++i) {
+    int t = cand[i];
+    bool gone = in_sorted(c.sup_sorted, c.n_sup, t) || (r.bsup && in_sorted(c.bsup_sorted, c.n_bsup, t));
+    if (!gone) zs[nz++] = t;
+  }
+  return nz;
+}
+
+// n-th member (1-based) of a group of equal-weight items whose running mass
+// starting at `above` first reaches the target: >= target (cut) or > target
+// (draw).  Always in [1, cnt].
+__device__ __forceinline__ unsigned long long group_pick(unsigned long long above, unsigned long long w,
+                                                         unsigned long long cnt, unsigned long long target,
+                                                         bool strict) {
+  unsigned long long n;
+  if (w == 0ull) return cnt;
+  if (target < above) return 1ull;
+  unsigned long long need = target - above;
+  n = strict ? need / w + 1ull : (need + w - 1ull) / w;
+  if (n < 1ull) n = 1ull;
+  if (n > cnt) n = cnt;
+  return n;
+}
+
+// Mass target of the top-p cut: the smallest integer >= p * Z.
+__device__ __forceinline__ unsigned long long topp_target(float p, unsigned long long Z) {
+  double t = static_cast<double>(p) * static_cast<double>(Z);
+  unsigned long long T = static_cast<unsigned long long>(ceil(t));
+  return T > Z ? Z : T;
+}
+// Mass target of the draw: the largest integer <= u * S, u in [0, 1).
+__device__ __forceinline__ unsigned long long draw_target(float u, unsigned long long S) {
+  if (!(u >= 0.0f)) u = 0.0f;               // NaN or negative -> 0
+  if (u >= 1.0f) u = 0x1.fffffep-1f;        // largest float below 1
+  double t = static_cast<double>(u) * static_cast<double>(S);
+  unsigned long long T = static_cast<unsigned long long>(floor(t));
+  return (T >= S && S > 0) ? S - 1 : T;
+}
+
+// ---------------------------------------------------------------------------
+// Warp-parallel search over N buckets (run by one full warp): the first
+// bucket, in scan order (descending bucket index when `desc`), at which the
+// running sum of v reaches `reached(cum)`.  `cnt` marks non-empty buckets;
+// when the sum never reaches the target the last non-empty bucket is
+// returned with found = 0.
+// ---------------------------------------------------------------------------
+template <class T>
+struct FindOut {
+  int b;          // bucket
+  T before;       // sum of v over buckets before b in scan order
+  int found;
+};
+
+template <int N, class T, class Reached>
+__device__ __forceinline__ FindOut<T> warp_find(const T* v, const unsigned* cnt, bool desc, Reached reached) {
+  constexpr int PER = N / 32;
+  const int lane = threadIdx.x & 31;
+  T local = 0;
+  int last_ne = -1;
+#pragma unroll 8
+  for (int j = 0; j < PER; ++j) {
+    const int p = lane * PER + j;
+    const int b = desc ? N - 1 - p : p;
+    local += v[b];
+    if (cnt[b]) last_ne = p;
+  }
+  T incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const T excl = incl - local;
+  FindOut<T> r;
+  r.b = 0;
+  r.before = 0;
+  r.found = 0;
+  const unsigned hit = __ballot_sync(0xffffffffu, reached(incl));
+  if (hit) {
+    const int L = __ffs(hit) - 1;
+    int b = 0;
+    T cum = 0;
+    if (lane == L) {
+      cum = excl;
+      for (int j = 0; j < PER; ++j) {
+        const int p = lane * PER + j;
+        b = desc ? N - 1 - p : p;
+        const T nx = cum + v[b];
+        if (reached(nx)) break;
+        cum = nx;
+      }
+    }
+    r.b = __shfl_sync(0xffffffffu, b, L);
+    r.before = __shfl_sync(0xffffffffu, cum, L);
+    r.found = 1;
+  } else {
+    const unsigned ne = __ballot_sync(0xffffffffu, last_ne >= 0);
+    if (ne) {
+      const int L = 31 - __clz(ne);
+      const int p = __shfl_sync(0xffffffffu, last_ne, L);
+      const int b = desc ? N - 1 - p : p;
+      // sum of v strictly before position p in scan order
+      T part = 0;
+      for (int j = 0; j < PER; ++j) {
+        const int q = lane * PER + j;
+        if (q < p) part += v[desc ? N - 1 - q : q];
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      r.b = b;
+      r.before = part;
+    }
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Radix selection engine.  A Source visits every item (score s, index i) of
+// one row, once per pass, on all threads of the CTA:
+//     src.pass([&](float s, unsigned i) { ... });
+// Items are ordered by (s desc, i asc).  Weights are wfix(s, m).
+// ---------------------------------------------------------------------------
+struct Hist {
+  unsigned long long mass[256];
+  unsigned cnt[256];
+  // broadcast slots
+  unsigned sel_bucket;
+  unsigned long long sel_above;
+  unsigned long long sel_mass;
+  unsigned sel_cnt;
+  unsigned sel_found;
+};
+
+// Kept-set filter: key >= klo, and, when `cut` is set, (key > kcut) or
+// (key == kcut and i <= icut).
+struct KeepFilter {
+  unsigned klo;
+  bool cut;
+  unsigned kcut, icut;
+  __device__ __forceinline__ bool operator()(unsigned key, unsigned i) const {
+    if (key < klo) return false;
+    if (!cut) return true;
+    return key > kcut || (key == kcut && i <= icut);
+  }
+};
+
+struct MassSel {
+  unsigned key;               // key of the selected item
+  unsigned idx;               // its index
+  unsigned long long mass;    // running mass up to and including it
+  bool found;
+};
+
+// Clear the histogram (all threads) -- followed by a barrier.
+__device__ __forceinline__ void hist_clear(Hist* h) {
+  for (int i = threadIdx.x; i < 256; i += kThreads) { h->mass[i] = 0ull; h->cnt[i] = 0u; }
+  __syncthreads();
+}
+
+// The rank-th smallest index (1-based) among items with key == key and
+// passing flt.  Counting radix select over the index bits, high digit first.
+template <class Src, class Flt>
+__device__ unsigned nth_index(const Src& src, Flt flt, unsigned key, unsigned rank, Hist* h) {
+  unsigned prefix = 0u;
+  for (int shift = 16; shift >= 0; shift -= 8) {
+    hist_clear(h);
+    const unsigned hi_mask = shift == 16 ? 0u : (0xffffffffu << (shift + 8));
+    src.pass([&](float s, unsigned i) {
+      unsigned k = fkey(s);
+      if (k == key && flt(k, i) && (i & hi_mask) == prefix) atomicAdd(&h->cnt[(i >> shift) & 255u], 1u);
+    });
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const unsigned need = rank;
+      FindOut<unsigned> f = warp_find<256>(h->cnt, h->cnt, false, [need](unsigned c) { return c >= need; });
+      if (threadIdx.x == 0) { h->sel_bucket = static_cast<unsigned>(f.b); h->sel_cnt = f.before; }
+    }
+    __syncthreads();
+    rank -= h->sel_cnt;
+    prefix |= h->sel_bucket << shift;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// The k-th largest key (with multiplicity) among items passing flt.
+template <class Src, class Flt>
+__device__ unsigned kth_key(const Src& src, Flt flt, unsigned k, Hist* h) {
+  unsigned prefix = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist_clear(h);
+    const unsigned hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
+    src.pass([&](float s, unsigned i) {
+      unsigned key = fkey(s);
+      if (flt(key, i) && (key & hi_mask) == prefix) atomicAdd(&h->cnt[(key >> shift) & 255u], 1u);
+    });
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const unsigned need = k;
+      FindOut<unsigned> f = warp_find<256>(h->cnt, h->cnt, true, [need](unsigned c) { return c >= need; });
+      if (threadIdx.x == 0) { h->sel_bucket = static_cast<unsigned>(f.b); h->sel_cnt = f.before; }
+    }
+    __syncthreads();
+    k -= h->sel_cnt;
+    prefix |= h->sel_bucket << shift;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// First item, in (s desc, i asc) order among items passing flt, at which
+// the running mass reaches the target: >= target (strict == false) or
+// > target (strict == true).  found == false when the filtered mass never
+// reaches it (the last item is returned then).
+template <class Src, class Flt>
+__device__ MassSel mass_select(const Src& src, Flt flt, float m, unsigned long long target, bool strict,
+                               Hist* h) {
+  unsigned prefix = 0u;
+  unsigned long long above = 0ull;
+  unsigned long long gmass = 0ull;
+  unsigned gcnt = 0u;
+  bool found = true;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist_clear(h);
+    const unsigned hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
+    src.pass([&](float s, unsigned i) {
+      unsigned key = fkey(s);
+      if (flt(key, i) && (key & hi_mask) == prefix) {
+        unsigned b = (key >> shift) & 255u;
+        atomicAdd(&h->mass[b], wfix(s, m));
+        atomicAdd(&h->cnt[b], 1u);
+      }
+    });
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const unsigned long long base = above;
+      const unsigned long long tgt = target;
+      FindOut<unsigned long long> f = warp_find<256>(
+          h->mass, h->cnt, true,
+          [base, tgt, strict](unsigned long long c) { return strict ? base + c > tgt : base + c >= tgt; });
+      if (threadIdx.x == 0) {
+        h->sel_bucket = static_cast<unsigned>(f.b);
+        h->sel_above = above + f.before;
+        h->sel_mass = h->mass[f.b];
+        h->sel_cnt = h->cnt[f.b];
+        h->sel_found = static_cast<unsigned>(f.found);
+      }
+    }
+    __syncthreads();
+    prefix |= h->sel_bucket << shift;
+    above = h->sel_above;
+    gmass = h->sel_mass;
+    gcnt = h->sel_cnt;
+    found = found && h->sel_found;
+    __syncthreads();
+  }
+  MassSel r;
+  r.key = prefix;
+  r.found = found && gcnt > 0u;
+  if (gcnt == 0u) { r.idx = 0u; r.mass = above; return r; }
+  unsigned long long w = gmass / gcnt;  // every item of the group has the same weight
+  unsigned long long n = r.found ? group_pick(above, w, gcnt, target, strict) : gcnt;
+  r.idx = nth_index(src, flt, prefix, static_cast<unsigned>(n), h);
+  r.mass = above + n * w;
+  return r;
+}
+
+// Sum of weights over items passing flt.
+template <class Src, class Flt>
+__device__ unsigned long long mass_sum(const Src& src, Flt flt, float m, RedScratch* red) {
+  unsigned long long acc = 0ull;
+  src.pass([&](float s, unsigned i) {
+    unsigned key = fkey(s);
+    if (flt(key, i)) acc += wfix(s, m);
+  });
+  return block_sum_u64(acc, red);
+}
+
+template <class Src, class Flt>
+__device__ unsigned count_items(const Src& src, Flt flt, RedScratch* red) {
+  unsigned acc = 0u;
+  src.pass([&](float s, unsigned i) {
+    if (flt(fkey(s), i)) ++acc;
+  });
+  return static_cast<unsigned>(block_sum_u64(acc, red));
+}
+
+// Full sampling selection over a source holding EVERY token of the row:
+// top_k, top_p, then the draw.  m = the row's maximum score.
+// Returns the drawn token, and (optionally) the kept-set filter and its mass.
+template <class Src>
+__device__ unsigned sample_exact(const DevCfg& c, const Src& src, float m, float u, unsigned V,
+                                 Hist* h, RedScratch* red, KeepFilter* kept_out,
+                                 unsigned long long* S_out) {
+  KeepFilter f{0u, false, 0u, 0u};
+  if (c.top_k > 0 && static_cast<unsigned>(c.top_k) < V)
+    f.klo = kth_key(src, f, static_cast<unsigned>(c.top_k), h);
+  unsigned long long Z = mass_sum(src, f, m, red);
+  unsigned long long S = Z;
+  if (c.top_p < 1.0f) {
+    unsigned long long T = topp_target(c.top_p, Z);
+    MassSel cut = mass_select(src, f, m, T, false, h);
+    f.cut = true;
+    f.kcut = cut.key;
+    f.icut = cut.idx;
+    S = cut.mass;
+  }
+  unsigned long long Td = draw_target(u, S);
+  MassSel d = mass_select(src, f, m, Td, true, h);
+  if (kept_out) *kept_out = f;
+  if (S_out) *S_out = S;
+  return d.idx;
+}
+
+}  // namespace tg

@@ -1,0 +1,259 @@
+"""Python binding of libtg (include/tg.h): argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of libtg.so.  This
+module turns torch CUDA tensors into device pointers, passes the current
+stream, and raises :class:`TGError` on a non-zero status.  It never computes
+a result itself; if the library is missing it raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_uint32, c_uint64, c_void_p
+
+from . import _build
+
+TG_OK = 0
+TG_ERR_INVALID_ARGUMENT = -1
+TG_ERR_UNSUPPORTED = -2
+TG_ERR_CUDA = -3
+TG_ERR_OUT_OF_MEMORY = -4
+
+TG_DTYPE_F32, TG_DTYPE_BF16 = 0, 1
+TG_GREEDY, TG_SAMPLE = 0, 1
+
+TG_FLAG_HISTORY_ID_OUT_OF_RANGE = 0x1
+TG_FLAG_BAD_ROW = 0x2
+TG_FLAG_SLOW_PATH = 0x4
+TG_MAX_VOCAB = 1 << 18
+
+# Names of every entry point declared in include/tg.h.
+EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_verify",
+           "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
+           "tg_status_string")
+
+
+class TGError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, status_string(status)))
+
+
+class tg_params(ctypes.Structure):
+    _fields_ = [
+        ("vocab", c_int32),
+        ("logits_dtype", c_int),
+        ("mode", c_int),
+        ("repetition_penalty", c_float),
+        ("no_repeat_ngram_size", c_int32),
+        ("bad_words_ids", POINTER(c_int32)),
+        ("n_bad_words_ids", c_int32),
+        ("suppress_tokens", POINTER(c_int32)),
+        ("n_suppress_tokens", c_int32),
+        ("begin_suppress_tokens", POINTER(c_int32)),
+        ("n_begin_suppress_tokens", c_int32),
+        ("eos_token_ids", POINTER(c_int32)),
+        ("n_eos_token_ids", c_int32),
+        ("min_length", c_int32),
+        ("min_new_tokens", c_int32),
+        ("forced_bos_token_id", c_int32),
+        ("forced_eos_token_ids", POINTER(c_int32)),
+        ("n_forced_eos_token_ids", c_int32),
+        ("max_new_tokens", c_int32),
+        ("temperature", c_float),
+        ("top_k", c_int32),
+        ("top_p", c_float),
+        ("max_batch", c_int32),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: str | None = None):
+    """Load libtg.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError("libtg.so is not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    lib.tg_params_init.argtypes = [POINTER(tg_params), c_int32]
+    lib.tg_params_init.restype = None
+    lib.tg_config_create.argtypes = [POINTER(tg_params), POINTER(c_void_p)]
+    lib.tg_config_destroy.argtypes = [c_void_p]
+    lib.tg_select.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                              c_void_p, c_void_p]
+    lib.tg_verify.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                              c_void_p, c_void_p]
+    lib.tg_process.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                               c_void_p, c_void_p, c_void_p]
+    lib.tg_query_status.argtypes = [c_void_p, POINTER(c_uint32), POINTER(c_uint64)]
+    lib.tg_clear_status.argtypes = [c_void_p]
+    lib.tg_next_num_candidates.argtypes = [c_int32, c_int32, c_int32]
+    lib.tg_next_num_candidates.restype = c_int32
+    lib.tg_status_string.argtypes = [c_int]
+    lib.tg_status_string.restype = c_char_p
+    for fn in ("tg_config_create", "tg_config_destroy", "tg_select", "tg_verify", "tg_process",
+               "tg_query_status", "tg_clear_status"):
+        getattr(lib, fn).restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().tg_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != TG_OK:
+        raise TGError(fn, status)
+
+
+def _ids(seq):
+    seq = [int(t) for t in (seq or ())]
+    arr = (c_int32 * max(1, len(seq)))(*seq) if seq else None
+    return arr, len(seq)
+
+
+def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalty=1.0,
+                no_repeat_ngram_size=0, bad_words_ids=(), suppress_tokens=(), begin_suppress_tokens=(),
+                eos_token_ids=(), min_length=0, min_new_tokens=0, forced_bos_token_id=-1,
+                forced_eos_token_ids=(), max_new_tokens=0, temperature=1.0, top_k=0, top_p=1.0,
+                max_batch=0):
+    """A filled tg_params plus the ctypes arrays its pointers refer to."""
+    lib = load_library()
+    p = tg_params()
+    lib.tg_params_init(ctypes.byref(p), int(vocab))
+    p.logits_dtype = {"f32": TG_DTYPE_F32, "bf16": TG_DTYPE_BF16}[logits_dtype] if isinstance(logits_dtype, str) else int(logits_dtype)
+    p.mode = {"greedy": TG_GREEDY, "sample": TG_SAMPLE}[mode] if isinstance(mode, str) else int(mode)
+    p.repetition_penalty = float(repetition_penalty)
+    p.no_repeat_ngram_size = int(no_repeat_ngram_size)
+    keep = []
+    for name, seq in (("bad_words_ids", bad_words_ids), ("suppress_tokens", suppress_tokens),
+                      ("begin_suppress_tokens", begin_suppress_tokens), ("eos_token_ids", eos_token_ids),
+                      ("forced_eos_token_ids", forced_eos_token_ids)):
+        arr, n = _ids(seq)
+        keep.append(arr)
+        setattr(p, name, ctypes.cast(arr, POINTER(c_int32)) if arr is not None else None)
+        setattr(p, "n_" + name, n)
+    p.min_length = int(min_length)
+    p.min_new_tokens = int(min_new_tokens)
+    p.forced_bos_token_id = int(forced_bos_token_id)
+    p.max_new_tokens = int(max_new_tokens)
+    p.temperature = float(temperature)
+    p.top_k = int(top_k)
+    p.top_p = float(top_p)
+    p.max_batch = int(max_batch)
+    return p, keep
+
+
+class Config:
+    """Owns a tg_config* (tg_config_create / tg_config_destroy)."""
+
+    def __init__(self, **params):
+        lib = load_library()
+        p, keep = make_params(**params)
+        h = c_void_p()
+        _check("tg_config_create", lib.tg_config_create(ctypes.byref(p), ctypes.byref(h)))
+        self.handle = h
+        self.params = dict(params)
+        del keep
+
+    def close(self):
+        if self.handle:
+            load_library().tg_config_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _ptr(t, name, dtypes=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError("%s is required" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    return c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+def _logit_dtypes():
+    import torch
+    return (torch.float32, torch.bfloat16, torch.int16, torch.uint16)
+
+
+def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms, out_ids, stream=None):
+    import torch
+    B, V = int(logits.shape[0]), int(logits.shape[-1])
+    st = load_library().tg_select(
+        _ptr(logits, "logits", _logit_dtypes()), B, V,
+        _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
+        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+        cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
+        _ptr(out_ids, "out_ids", (torch.int32,)), _stream(stream))
+    _check("tg_select", st)
+    return out_ids
+
+
+def tg_verify(target_logits, cand_ids, K: int, cfg: Config, uniforms, out_match, out_next, stream=None):
+    import torch
+    B, V = int(target_logits.shape[0]), int(target_logits.shape[-1])
+    st = load_library().tg_verify(
+        _ptr(target_logits, "target_logits", _logit_dtypes()), B, V, _ptr(cand_ids, "cand_ids", (torch.int32,)),
+        int(K), cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
+        _ptr(out_match, "out_match", (torch.int32,)), _ptr(out_next, "out_next", (torch.int32,)), _stream(stream))
+    _check("tg_verify", st)
+    return out_match, out_next
+
+
+def tg_process(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, out_scores, out_banbits=None,
+               out_probs=None, stream=None):
+    import torch
+    B, V = int(logits.shape[0]), int(logits.shape[-1])
+    st = load_library().tg_process(
+        _ptr(logits, "logits", _logit_dtypes()), B, V,
+        _ptr(hist_ids, "hist_ids", (torch.int32,)) if hist_ids is not None and hist_ids.numel() else None,
+        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+        cfg.handle, _ptr(out_scores, "out_scores", (torch.float32,)),
+        _ptr(out_banbits, "out_banbits", (torch.int32, torch.uint32), allow_none=True),
+        _ptr(out_probs, "out_probs", (torch.float32,), allow_none=True), _stream(stream))
+    _check("tg_process", st)
+
+
+def tg_query_status(cfg: Config):
+    f, s = c_uint32(), c_uint64()
+    _check("tg_query_status", load_library().tg_query_status(cfg.handle, ctypes.byref(f), ctypes.byref(s)))
+    return int(f.value), int(s.value)
+
+
+def tg_clear_status(cfg: Config):
+    _check("tg_clear_status", load_library().tg_clear_status(cfg.handle))
+
+
+def tg_next_num_candidates(K: int, n_match: int, K_max: int) -> int:
+    return int(load_library().tg_next_num_candidates(int(K), int(n_match), int(K_max)))
+
+
+def tg_status_string(status: int) -> str:
+    return status_string(status)

@@ -1,0 +1,82 @@
+"""tg_process (diagnostic) against the oracle: processed scores bit-exact
+(0 ULP), ban bits bit-exact, final probabilities within 1e-6 relative plus
+one fixed-point quantum (2^-44) absolute."""
+import numpy as np
+import pytest
+
+from logits_processing_token_gb300 import workloads as W
+from oracle import tg_oracle as O
+
+from .gpu_util import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from logits_processing_token_gb300 import _build
+    _build.build()
+
+
+def run_process(w):
+    import torch
+    import logits_processing_token_gb300 as tg
+    cfg = tg.Config(**w.params)
+    d = to_device(w)
+    nw = (w.V + 31) // 32
+    sc = torch.full((w.B, w.V), 123.0, device="cuda")
+    bb = torch.zeros((w.B, nw), dtype=torch.int32, device="cuda")
+    pr = torch.zeros((w.B, w.V), device="cuda")
+    tg.tg_process(d["logits"], d["hist_ids"], d["hist_offsets"], d["prompt_lens"], cfg, sc, bb, pr)
+    torch.cuda.synchronize()
+    return sc.cpu().numpy(), bb.cpu().numpy().view(np.uint32), pr.cpu().numpy()
+
+
+def check(w, rows=None):
+    sc, bb, pr = run_process(w)
+    p = O.Params(**w.params)
+    rows = range(w.B) if rows is None else rows
+    for b in rows:
+        h = list(w.history(b))
+        if not h:
+            assert np.all(sc[b] == 123.0)
+            continue
+        x = O.upcast_row(w.logits[b], p.logits_dtype)
+        s_ref, banned = O.processed_scores(x, h, int(w.prompt_lens[b]), p)
+        assert np.array_equal(sc[b].view(np.uint32) & 0x7fffffff, s_ref.view(np.uint32) & 0x7fffffff), b
+        assert np.array_equal(sc[b], s_ref), b
+        bits = np.unpackbits(bb[b].view(np.uint8), bitorder="little")[:w.V].astype(bool)
+        assert np.array_equal(bits, banned), b
+        if p.mode == "sample":
+            _, _, _, _, info = O.sample_distribution(s_ref, p)
+            if info.topp_boundary:
+                continue
+            ref = O.final_distribution(s_ref, p)
+        else:
+            ref = O.softmax64(s_ref)
+        tol = 1e-6 * ref + 2.0 ** -44
+        assert np.all(np.abs(pr[b].astype(np.float64) - ref) <= tol), (b, np.max(np.abs(pr[b] - ref) - tol))
+
+
+def test_process_config2():
+    check(W.config2(B=16))
+
+
+def test_process_config3():
+    check(W.config3(B=16))
+
+
+def test_process_config5():
+    check(W.config5(B=4, L_max=2048))
+
+
+def test_process_config1():
+    check(W.config1())
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_process_random(seed):
+    w = W.random_case(seed, B=8, V=997, dtype="bf16" if seed % 2 else "f32", mode="sample",
+                      repetition_penalty=1.4, no_repeat_ngram_size=2, temperature=0.6, top_k=50, top_p=0.8,
+                      eos_token_ids=[1], min_new_tokens=3, suppress_tokens=[4, 5])
+    check(w)

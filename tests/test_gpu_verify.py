@@ -1,0 +1,83 @@
+"""tg_verify on the GPU against the oracle's verify (Assisted Generation,
+steps 3-5), for B in {1, 8, 32} and K from 1 to 16, greedy and sampling."""
+import numpy as np
+import pytest
+
+from logits_processing_token_gb300 import workloads as W
+from oracle import tg_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from logits_processing_token_gb300 import _build
+    _build.build()
+
+
+def make_case(B, K, mode, **ov):
+    w = W.config4(B=B, K=K, mode=mode)
+    w.params.update(ov)
+    tgt = w.extra["target"]
+    p = O.Params(**w.params)
+    # the agreeing candidates copy the target's greedy token (oracle argmax)
+    greedy = np.array([[O.select_row(tgt[b, j], [0], 1, O.Params(vocab=w.V), 0.0)[0] for j in range(K)]
+                       for b in range(B)])
+    cand = W.make_candidates(greedy, w.extra["agree"], w.extra["offsets"], w.V)
+    return w, tgt, cand, p
+
+
+def run_gpu(w, tgt, cand, K):
+    import torch
+    import logits_processing_token_gb300 as tg
+    cfg = tg.Config(**w.params, max_batch=64)
+    t = torch.from_numpy(np.ascontiguousarray(tgt)).cuda()
+    c = torch.from_numpy(cand).cuda()
+    u = torch.from_numpy(np.ascontiguousarray(w.uniforms)).cuda()
+    om = torch.full((w.B,), -9, dtype=torch.int32, device="cuda")
+    on = torch.full((w.B, K + 1), -9, dtype=torch.int32, device="cuda")
+    tg.tg_verify(t, c, K, cfg, u, om, on)
+    torch.cuda.synchronize()
+    return om.cpu().numpy(), on.cpu().numpy(), cfg
+
+
+@pytest.mark.parametrize("B", [1, 8, 32])
+@pytest.mark.parametrize("K", [1, 5, 16])
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_verify_parity(B, K, mode):
+    w, tgt, cand, p = make_case(B, K, mode)
+    om, on, _ = run_gpu(w, tgt, cand, K)
+    m_ref, n_ref, infos = O.verify(tgt, cand, K, p, w.uniforms)
+    for b in range(B):
+        nxt, row_infos = infos[b]
+        # a row is decided once every position up to its first mismatch is off any CDF boundary
+        upto = int(m_ref[b])
+        if any(ri.u_boundary or ri.topp_boundary for ri in row_infos[:upto + 1]):
+            continue
+        assert om[b] == m_ref[b], (b, om[b], m_ref[b])
+        assert list(on[b]) == list(n_ref[b]), (b, on[b], n_ref[b])
+
+
+def test_verify_warpers_and_repeat():
+    # temperature/top_k/top_p apply per position; repeated calls reuse the tickets
+    w, tgt, cand, p = make_case(8, 4, "sample", temperature=0.7, top_k=40, top_p=0.9)
+    om1, on1, cfg = run_gpu(w, tgt, cand, 4)
+    om2, on2, _ = run_gpu(w, tgt, cand, 4)
+    assert np.array_equal(om1, om2) and np.array_equal(on1, on2)
+    m_ref, n_ref, infos = O.verify(tgt, cand, 4, p, w.uniforms)
+    for b in range(8):
+        if any(ri.u_boundary or ri.topp_boundary for ri in infos[b][1]):
+            continue
+        assert om1[b] == m_ref[b] and list(on1[b]) == list(n_ref[b])
+
+
+def test_candidate_heuristic_trace():
+    import logits_processing_token_gb300 as tg
+    K = O.INITIAL_NUM_CANDIDATES
+    trace = []
+    for n in (5, 7, 3, 0, 6, 6):
+        K2 = tg.tg_next_num_candidates(K, min(n, K), 16)
+        assert K2 == O.next_num_candidates(K, min(n, K), 16)
+        trace.append(K2)
+        K = K2
+    assert trace[:2] == [7, 9]
