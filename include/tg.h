@@ -182,6 +182,39 @@ tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hi
                      const tg_config* cfg, float* out_scores, uint32_t* out_banbits,
                      float* out_probs, tg_stream stream);
 
+/* Largest B that tg_verify_noalloc takes. */
+#define TG_NOALLOC_MAX_BATCH 1024
+
+/*
+ * tg_verify_noalloc -- tg_verify for callers that cannot allocate device
+ * memory.  (An addition of this library; the pages have no counterpart.)
+ *
+ * Some callers may not call cudaMalloc: a serving engine that gives all of
+ * HBM to its KV-cache pool at start-up and forbids later allocations, or a
+ * pipelined decode step where an allocation would synchronise the device.
+ * They cannot create a tg_config either, so this entry point takes the
+ * settings in *params by value (only vocab, logits_dtype, mode, temperature,
+ * top_k and top_p are read; as in tg_verify, no history processor runs) and
+ * keeps its per-row tickets in a fixed array in the library's own device
+ * memory (TG_NOALLOC_MAX_BATCH + 4 words per device, held until the process
+ * exits).  A call allocates nothing.
+ *
+ * Arguments, layouts and outputs are those of tg_verify.  Errors:
+ * TG_ERR_UNSUPPORTED when B > TG_NOALLOC_MAX_BATCH or V > TG_MAX_VOCAB;
+ * TG_ERR_INVALID_ARGUMENT for a bad setting or pointer; TG_ERR_CUDA when the
+ * set-up or the launch fails.  Device-side status bits of this entry point
+ * are not reported.
+ *
+ * The first call on a device does a one-time synchronous set-up on the
+ * current device (it resolves the array's address and zeroes it); make that
+ * first call before any stream capture.  Each call clears the tickets it
+ * uses on `stream`.  All calls on a device share the one array: calls that
+ * overlap on the GPU (different streams without ordering) race on it.
+ */
+tg_status tg_verify_noalloc(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids,
+                            int32_t K, const tg_params* params, const float* uniforms, int32_t* out_match,
+                            int32_t* out_next, tg_stream stream);
+
 /* Read (synchronously) the sticky status bits and the count of rows that took
  * the multi-pass exact path since the last clear. */
 tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_rows);

@@ -19,6 +19,9 @@
 // is exact whenever the candidates hold the k largest scores (top_k) or more
 // mass than the cut (top_p) or the draw target needs.  A row where that check
 // fails runs the multi-pass exact selection over the whole row instead.
+#include <mutex>
+
+#include "../../include/tg.h"
 #include "tg_device.cuh"
 
 namespace tg {
@@ -1190,6 +1193,127 @@ extern "C" int tg_debug_set(double* p) { return (int)cudaMemcpyToSymbol(g_dbg, &
 // ---------------------------------------------------------------------------
 // host-side launch helpers (C++ linkage, used by tg_api.cu)
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// tg_verify_noalloc: the verify step for callers that may not allocate.
+//
+// tg_verify keeps its per-row tickets in memory that tg_config_create
+// allocates.  Some callers cannot allocate device memory at all: a serving
+// engine that hands every byte of HBM to its KV-cache pool at start-up and
+// forbids later allocations, or a decode loop where a cudaMalloc would
+// synchronise the device in the middle of a pipelined step.  This variant
+// takes the settings by value and keeps its tickets in a fixed array in the
+// library's own device memory, so a call allocates nothing.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxBatch = TG_NOALLOC_MAX_BATCH;
+// tickets [kNoAllocMaxBatch], then the status word, a pad and the slow-row counter
+constexpr int kNoAllocWords = kNoAllocMaxBatch + 4;
+
+// Shared by every tg_verify_noalloc call on a device; holds what the last
+// call left (the tickets are cleared at the start of each call).  Every GPU
+// that loads the library keeps this array until the process exits.
+static __device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocWords];
+
+struct NoAllocDevice {
+  bool ready;
+  unsigned* scratch;   // device address of g_noalloc_scratch on this device
+  int nsm;
+  int nstage[2], smem[2], bps[2];   // launch plan per dtype
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: resolve the scratch array's
+// device address, zero it, and plan the verify launch.
+cudaError_t noalloc_setup(int dev, NoAllocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(p, 0, sizeof(g_noalloc_scratch));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev);
+    int optin = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    for (int dt = 0; dt < 2 && e == cudaSuccess; ++dt) {
+      const int ns = min(8, (optin - select_smem_bytes(0, 0)) / kStageBytes);
+      d.nstage[dt] = ns;
+      d.smem[dt] = select_smem_bytes(ns, 0);
+      e = select_occupancy(dt, true, d.smem[dt], &d.bps[dt]);
+      if (e == cudaSuccess && (ns < 2 || d.bps[dt] < 1)) e = cudaErrorInvalidConfiguration;
+      d.bps[dt] = 1;
+    }
+    if (e != cudaSuccess) return e;
+    d.scratch = static_cast<unsigned*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace tg
+
+extern "C" tg_status tg_verify_noalloc(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids,
+                                       int32_t K, const tg_params* params, const float* uniforms,
+                                       int32_t* out_match, int32_t* out_next, tg_stream stream) {
+  using namespace tg;
+  if (!params || V != params->vocab || V < 1 || B < 0 || K < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (V > TG_MAX_VOCAB) return TG_ERR_UNSUPPORTED;
+  if (params->logits_dtype != TG_DTYPE_F32 && params->logits_dtype != TG_DTYPE_BF16) return TG_ERR_INVALID_ARGUMENT;
+  if (params->mode != TG_GREEDY && params->mode != TG_SAMPLE) return TG_ERR_INVALID_ARGUMENT;
+  if (!(params->temperature > 0.0f) || !(params->temperature < INFINITY)) return TG_ERR_INVALID_ARGUMENT;
+  if (params->top_k < 0 || !(params->top_p > 0.0f && params->top_p <= 1.0f)) return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (B > kNoAllocMaxBatch) return TG_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * (K + 1) > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
+  if (!target_logits || !cand_ids || !out_match || !out_next) return TG_ERR_INVALID_ARGUMENT;
+  if (params->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return TG_ERR_CUDA;
+  NoAllocDevice* d = nullptr;
+  if (noalloc_setup(dev, &d) != cudaSuccess) return TG_ERR_CUDA;
+
+  DevCfg c;
+  memset(&c, 0, sizeof(c));
+  c.V = V;
+  c.dtype = params->logits_dtype;
+  c.mode = params->mode;
+  c.rho = 1.0f;
+  c.bos = -1;
+  c.temp = params->temperature;
+  c.top_k = params->top_k;
+  c.top_p = params->top_p;
+  c.tickets = d->scratch;
+  c.status = d->scratch + kNoAllocMaxBatch;
+  c.slow_rows = reinterpret_cast<unsigned long long*>(d->scratch + kNoAllocMaxBatch + 2);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the tickets of this call start at zero
+  if (cudaMemsetAsync(c.tickets, 0, static_cast<size_t>(B) * sizeof(unsigned), s) != cudaSuccess) return TG_ERR_CUDA;
+
+  SelArgs a;
+  memset(&a, 0, sizeof(a));
+  a.logits = target_logits;
+  a.nrows = B * (K + 1);
+  a.V = V;
+  a.uniforms = uniforms;
+  a.out = out_next;
+  a.cand = cand_ids;
+  a.K = K;
+  a.out_match = out_match;
+  const int dt = c.dtype == kBF16 ? 1 : 0;
+  a.nstage = d->nstage[dt];
+  a.nwords = 0;
+  const int grid = static_cast<int>(min(static_cast<long long>(a.nrows), static_cast<long long>(d->bps[dt]) * d->nsm));
+  return launch_select(c, a, true, grid, d->smem[dt], s) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+namespace tg {
+
 int select_smem_bytes(int nstage, int nwords) {
   return sel_fixed_bytes() + 2 * bitmap_bytes(nwords) + nstage * kStageBytes;
 }

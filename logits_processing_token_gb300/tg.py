@@ -30,7 +30,8 @@ TG_MAX_VOCAB = 1 << 18
 # Names of every entry point declared in include/tg.h.
 EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
-           "tg_status_string")
+           "tg_status_string", "tg_verify_noalloc")
+TG_NOALLOC_MAX_BATCH = 1024
 
 
 class TGError(RuntimeError):
@@ -91,6 +92,9 @@ def load_library(path: str | None = None):
                               c_void_p, c_void_p]
     lib.tg_verify.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p]
+    lib.tg_verify_noalloc.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, POINTER(tg_params), c_void_p,
+                                      c_void_p, c_void_p, c_void_p]
+    lib.tg_verify_noalloc.restype = c_int
     lib.tg_process.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_void_p]
     lib.tg_query_status.argtypes = [c_void_p, POINTER(c_uint32), POINTER(c_uint64)]
