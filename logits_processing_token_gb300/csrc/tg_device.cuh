@@ -14,9 +14,8 @@ namespace tg {
 
 constexpr int kThreads = 512;               // threads per CTA of every kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageBytes = 16384;          // one TMA bulk copy / sub-chunk of a row
-constexpr int kCandCap = 6144;              // candidate slots of the one-pass path
-constexpr int kSpecCap = 512;               // bf16 side list of patched tokens per sub-chunk
+constexpr int kStageBytes = 32768;          // one TMA bulk copy / sub-chunk of a row
+constexpr int kCandCap = 4096;              // candidate slots of the one-pass path
 constexpr float kFilter = -3.40282346638528859812e+38f;  // -FLT_MAX
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr int kFixShift = 44;               // fixed-point mass: weight * 2^44, weight <= 1
@@ -88,6 +87,10 @@ cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_s
 // ---------------------------------------------------------------------------
 // small helpers
 // ---------------------------------------------------------------------------
+// Barrier over the kThreads "consumer" threads only (named barrier 1).  The
+// select kernel adds one producer warp that never takes part.
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
 }
@@ -130,6 +133,22 @@ __device__ __forceinline__ unsigned long long wfix(float s, float m) {
   return __float2ull_rn(w * 17592186044416.0f);
 }
 
+// Fast weight in fixed point: the one-pass path's weight, consistent with
+// the excluded mass it accumulates with wfast (cc = m * log2e).
+__device__ __forceinline__ unsigned long long wfix_fast(float s, float cc) {
+  return __float2ull_rn(wfast(s, cc) * 17592186044416.0f);
+}
+
+// Weight functors for the radix engine.
+struct WExact {
+  float m;
+  __device__ __forceinline__ unsigned long long operator()(float s) const { return wfix(s, m); }
+};
+struct WFast {
+  float cc;
+  __device__ __forceinline__ unsigned long long operator()(float s) const { return wfix_fast(s, cc); }
+};
+
 // Temperature, then the clamp at the filter value.  A patched slot holding
 // -inf stays -inf (it is counted through its side-list entry instead).
 __device__ __forceinline__ float temper(float v, float T) {
@@ -165,18 +184,18 @@ struct RedScratch {
 
 __device__ __forceinline__ float block_max(float v, RedScratch* r) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) r->f[threadIdx.x >> 5] = v;
-  __syncthreads();
+  csync();
   float m = r->f[0];
   for (int i = 1; i < kWarps; ++i) m = fmaxf(m, r->f[i]);
   return m;
 }
 __device__ __forceinline__ float block_sum_f(float v, RedScratch* r) {
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) r->f[threadIdx.x >> 5] = v;
-  __syncthreads();
+  csync();
   // pairwise over the 16 warp partials
   float a[kWarps];
 #pragma unroll
@@ -193,9 +212,9 @@ __device__ __forceinline__ void block_max_sum(float& m, float& e, RedScratch* r)
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     e += __shfl_xor_sync(0xffffffffu, e, o);
   }
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) { r->f[threadIdx.x >> 5] = m; r->u[threadIdx.x >> 5] = __float_as_uint(e); }
-  __syncthreads();
+  csync();
   float a[kWarps];
   float mm = r->f[0];
 #pragma unroll
@@ -209,36 +228,36 @@ __device__ __forceinline__ void block_max_sum(float& m, float& e, RedScratch* r)
 }
 __device__ __forceinline__ double block_sum_d(double v, RedScratch* r) {
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) r->d[threadIdx.x >> 5] = v;
-  __syncthreads();
+  csync();
   double s = 0.0;
   for (int i = 0; i < kWarps; ++i) s += r->d[i];
   return s;
 }
 __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, RedScratch* r) {
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) r->q[threadIdx.x >> 5] = v;
-  __syncthreads();
+  csync();
   unsigned long long s = 0;
   for (int i = 0; i < kWarps; ++i) s += r->q[i];
   return s;
 }
 __device__ __forceinline__ unsigned block_min_u(unsigned v, RedScratch* r) {
   for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) r->u[threadIdx.x >> 5] = v;
-  __syncthreads();
+  csync();
   unsigned m = r->u[0];
   for (int i = 1; i < kWarps; ++i) m = min(m, r->u[i]);
   return m;
 }
 __device__ __forceinline__ unsigned block_max_u(unsigned v, RedScratch* r) {
   for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
+  csync();
   if ((threadIdx.x & 31) == 0) r->u[threadIdx.x >> 5] = v;
-  __syncthreads();
+  csync();
   unsigned m = r->u[0];
   for (int i = 1; i < kWarps; ++i) m = max(m, r->u[i]);
   return m;
@@ -293,7 +312,7 @@ __device__ __forceinline__ void build_row_bitmaps(const DevCfg& c, const int32_t
                                   unsigned* H, unsigned* N, int nwords) {
   const int tid = threadIdx.x;
   for (int w = tid; w < nwords; w += kThreads) { H[w] = 0u; N[w] = 0u; }
-  __syncthreads();
+  csync();
   const int V = c.V;
   const int32_t* h = hist + r.h0;
   const int L = r.L;
@@ -333,7 +352,7 @@ __device__ __forceinline__ void build_row_bitmaps(const DevCfg& c, const int32_t
   if (r.bsup)
     for (int i = tid; i < c.n_bsup; i += kThreads) set_bit(N, __ldg(c.bsup_sorted + i));
   if (bad_id) atomicOr(c.status, kFlagBadId);
-  __syncthreads();
+  csync();
 }
 
 // Processed score of one token from its raw value and the row bitmaps
@@ -482,7 +501,8 @@ __device__ __forceinline__ FindOut<T> warp_find(const T* v, const unsigned* cnt,
 // Radix selection engine.  A Source visits every item (score s, index i) of
 // one row, once per pass, on all threads of the CTA:
 //     src.pass([&](float s, unsigned i) { ... });
-// Items are ordered by (s desc, i asc).  Weights are wfix(s, m).
+// Items are ordered by (s desc, i asc).  Weights come from a functor (WExact
+// or WFast) so that every pass of one selection uses the same weights.
 // ---------------------------------------------------------------------------
 struct Hist {
   unsigned long long mass[256];
@@ -518,7 +538,7 @@ struct MassSel {
 // Clear the histogram (all threads) -- followed by a barrier.
 __device__ __forceinline__ void hist_clear(Hist* h) {
   for (int i = threadIdx.x; i < 256; i += kThreads) { h->mass[i] = 0ull; h->cnt[i] = 0u; }
-  __syncthreads();
+  csync();
 }
 
 // The rank-th smallest index (1-based) among items with key == key and
@@ -533,16 +553,16 @@ __device__ unsigned nth_index(const Src& src, Flt flt, unsigned key, unsigned ra
       unsigned k = fkey(s);
       if (k == key && flt(k, i) && (i & hi_mask) == prefix) atomicAdd(&h->cnt[(i >> shift) & 255u], 1u);
     });
-    __syncthreads();
+    csync();
     if (threadIdx.x < 32) {
       const unsigned need = rank;
       FindOut<unsigned> f = warp_find<256>(h->cnt, h->cnt, false, [need](unsigned c) { return c >= need; });
       if (threadIdx.x == 0) { h->sel_bucket = static_cast<unsigned>(f.b); h->sel_cnt = f.before; }
     }
-    __syncthreads();
+    csync();
     rank -= h->sel_cnt;
     prefix |= h->sel_bucket << shift;
-    __syncthreads();
+    csync();
   }
   return prefix;
 }
@@ -558,16 +578,16 @@ __device__ unsigned kth_key(const Src& src, Flt flt, unsigned k, Hist* h) {
       unsigned key = fkey(s);
       if (flt(key, i) && (key & hi_mask) == prefix) atomicAdd(&h->cnt[(key >> shift) & 255u], 1u);
     });
-    __syncthreads();
+    csync();
     if (threadIdx.x < 32) {
       const unsigned need = k;
       FindOut<unsigned> f = warp_find<256>(h->cnt, h->cnt, true, [need](unsigned c) { return c >= need; });
       if (threadIdx.x == 0) { h->sel_bucket = static_cast<unsigned>(f.b); h->sel_cnt = f.before; }
     }
-    __syncthreads();
+    csync();
     k -= h->sel_cnt;
     prefix |= h->sel_bucket << shift;
-    __syncthreads();
+    csync();
   }
   return prefix;
 }
@@ -576,8 +596,8 @@ __device__ unsigned kth_key(const Src& src, Flt flt, unsigned k, Hist* h) {
 // the running mass reaches the target: >= target (strict == false) or
 // > target (strict == true).  found == false when the filtered mass never
 // reaches it (the last item is returned then).
-template <class Src, class Flt>
-__device__ MassSel mass_select(const Src& src, Flt flt, float m, unsigned long long target, bool strict,
+template <class Src, class Flt, class Wt>
+__device__ MassSel mass_select(const Src& src, Flt flt, Wt wf, unsigned long long target, bool strict,
                                Hist* h) {
   unsigned prefix = 0u;
   unsigned long long above = 0ull;
@@ -591,11 +611,11 @@ __device__ MassSel mass_select(const Src& src, Flt flt, float m, unsigned long l
       unsigned key = fkey(s);
       if (flt(key, i) && (key & hi_mask) == prefix) {
         unsigned b = (key >> shift) & 255u;
-        atomicAdd(&h->mass[b], wfix(s, m));
+        atomicAdd(&h->mass[b], wf(s));
         atomicAdd(&h->cnt[b], 1u);
       }
     });
-    __syncthreads();
+    csync();
     if (threadIdx.x < 32) {
       const unsigned long long base = above;
       const unsigned long long tgt = target;
@@ -610,13 +630,13 @@ __device__ MassSel mass_select(const Src& src, Flt flt, float m, unsigned long l
         h->sel_found = static_cast<unsigned>(f.found);
       }
     }
-    __syncthreads();
+    csync();
     prefix |= h->sel_bucket << shift;
     above = h->sel_above;
     gmass = h->sel_mass;
     gcnt = h->sel_cnt;
     found = found && h->sel_found;
-    __syncthreads();
+    csync();
   }
   MassSel r;
   r.key = prefix;
@@ -630,12 +650,12 @@ __device__ MassSel mass_select(const Src& src, Flt flt, float m, unsigned long l
 }
 
 // Sum of weights over items passing flt.
-template <class Src, class Flt>
-__device__ unsigned long long mass_sum(const Src& src, Flt flt, float m, RedScratch* red) {
+template <class Src, class Flt, class Wt>
+__device__ unsigned long long mass_sum(const Src& src, Flt flt, Wt wf, RedScratch* red) {
   unsigned long long acc = 0ull;
   src.pass([&](float s, unsigned i) {
     unsigned key = fkey(s);
-    if (flt(key, i)) acc += wfix(s, m);
+    if (flt(key, i)) acc += wf(s);
   });
   return block_sum_u64(acc, red);
 }
@@ -659,18 +679,19 @@ __device__ unsigned sample_exact(const DevCfg& c, const Src& src, float m, float
   KeepFilter f{0u, false, 0u, 0u};
   if (c.top_k > 0 && static_cast<unsigned>(c.top_k) < V)
     f.klo = kth_key(src, f, static_cast<unsigned>(c.top_k), h);
-  unsigned long long Z = mass_sum(src, f, m, red);
+  const WExact wx{m};
+  unsigned long long Z = mass_sum(src, f, wx, red);
   unsigned long long S = Z;
   if (c.top_p < 1.0f) {
     unsigned long long T = topp_target(c.top_p, Z);
-    MassSel cut = mass_select(src, f, m, T, false, h);
+    MassSel cut = mass_select(src, f, wx, T, false, h);
     f.cut = true;
     f.kcut = cut.key;
     f.icut = cut.idx;
     S = cut.mass;
   }
   unsigned long long Td = draw_target(u, S);
-  MassSel d = mass_select(src, f, m, Td, true, h);
+  MassSel d = mass_select(src, f, wx, Td, true, h);
   if (kept_out) *kept_out = f;
   if (S_out) *S_out = S;
   return d.idx;
