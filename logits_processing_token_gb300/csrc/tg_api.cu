@@ -222,6 +222,7 @@ tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* his
   tg::SelArgs a{};
   a.logits = logits;
   a.nrows = B;
+  a.nrows_total = B;
   a.V = V;
   a.hist = hist_ids;
   a.off = hist_offsets;
@@ -248,6 +249,7 @@ tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32
   tg::SelArgs a{};
   a.logits = target_logits;
   a.nrows = B * (K + 1);
+  a.nrows_total = a.nrows;
   a.V = V;
   a.uniforms = uniforms;
   a.out = out_next;
@@ -271,6 +273,7 @@ tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hi
   tg::SelArgs a{};
   a.logits = logits;
   a.nrows = B;
+  a.nrows_total = B;
   a.V = V;
   a.hist = hist_ids;
   a.off = hist_offsets;

@@ -62,7 +62,9 @@ struct DevCfg {
 
 struct SelArgs {
   const void* logits;
-  int nrows;             // B (select) or B*(K+1) (verify)
+  int nrows;             // rows of this launch end here (exclusive)
+  int row_begin;         // rows of this launch start here
+  int nrows_total;       // B (select) or B*(K+1) (verify): rows of the whole call
   int V;
   const int32_t* hist;
   const int64_t* off;
@@ -301,14 +303,15 @@ __device__ __forceinline__ RowMeta row_meta(const DevCfg& c, const int32_t* hist
 }
 
 // ---------------------------------------------------------------------------
-// Per-row bitmaps in shared memory: H = history ids (penalised, only when
-// rho != 1), N = banned (n-gram, bad words, eos under min length, suppress,
-// begin-suppress).  nwords = ceil(V/32).
+// Per-row bitmaps in shared memory: N = banned (n-gram, bad words, eos under
+// min length, suppress, begin-suppress); H = every token a processor changes:
+// the banned ones and, when rho != 1, the history ids.  A token of H that is
+// not in N is penalised.  nwords = ceil(V/32).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void set_bit(unsigned* bm, int t) { atomicOr(bm + (t >> 5), 1u << (t & 31)); }
 __device__ __forceinline__ bool get_bit(const unsigned* bm, int t) { return (bm[t >> 5] >> (t & 31)) & 1u; }
 
-__device__ __forceinline__ void build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
+static __device__ __noinline__ void build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
                                   unsigned* H, unsigned* N, int nwords) {
   const int tid = threadIdx.x;
   for (int w = tid; w < nwords; w += kThreads) { H[w] = 0u; N[w] = 0u; }
@@ -352,6 +355,9 @@ __device__ __forceinline__ void build_row_bitmaps(const DevCfg& c, const int32_t
   if (r.bsup)
     for (int i = tid; i < c.n_bsup; i += kThreads) set_bit(N, __ldg(c.bsup_sorted + i));
   if (bad_id) atomicOr(c.status, kFlagBadId);
+  csync();
+  // H becomes the marked set M = history | banned; N stays the banned set
+  for (int w = tid; w < nwords; w += kThreads) H[w] |= N[w];
   csync();
 }
 

@@ -1,32 +1,38 @@
 // Token-selection kernels for sm_103a.
 //
-//  select_kernel  -- tg_select and tg_verify.  One CTA per row at a time
-//                    (persistent over rows).  A producer warp streams every
-//                    row once from HBM with 32 KB TMA bulk copies into a ring
-//                    of shared-memory stages; 16 consumer warps each own a
-//                    fixed slice of every stage and process it on their own
-//                    (no CTA barrier while a row streams), releasing the
-//                    stage through an mbarrier.
+//  select_kernel  -- tg_select and tg_verify.  One CTA of 16 warps per SM,
+//                    persistent over the rows it owns.  Every row is streamed
+//                    once from HBM with 32 KB bulk copies (TMA) into a ring of
+//                    shared-memory stages.  Each warp copies its 2 KB slice of
+//                    a stage into registers and counts itself done; the last
+//                    of the 16 warps to do so refills the stage, so loads are
+//                    in flight while every warp computes on registers.
 //  process_kernel -- tg_process (diagnostic): processed scores, ban bits and
 //                    the final distribution, written to global memory.
 //
-// Processors.  Tokens that a history/ban bitmap marks are patched in the
-// stage before a warp reads its slice (f32: the processed score in place;
-// bf16: -inf in place and the exact f32 score in a per-warp side list).
+// Processors.  A per-row bitmap M marks every token that a processor changes
+// (history ids under a repetition penalty, n-gram bans, bad words, eos under
+// min length, suppress and begin-suppress ids); N marks the banned ones.
+// The streaming loop never computes a processed score: greedy treats marked
+// tokens as -inf, sampling counts their raw weight.  At the end of the row the
+// marked tokens are read again (from L2), processed exactly, and merged in:
+// greedy compares them with the best unmarked token, sampling replaces their
+// raw weight with the processed one.
 //
-// Sampling in one pass.  While streaming, every token's weight exp(s - m)
-// (m = the warp's reference maximum) either joins the warp's excluded mass E
-// (s below the warp's threshold theta) or the token joins the warp's
-// candidate segment (s >= theta).  At the end of the row every warp drops
-// candidates below the largest theta, so the candidates are exactly the
-// tokens with s >= theta_final and all others are in E.  top_k, the top_p cut
-// and the draw then run exactly on the candidates with fixed-point weights;
-// the excluded tokens all sit after every candidate in the (score desc,
-// index asc) order, so the result is exact whenever the candidates hold the
-// k largest scores (top_k) or more mass than the cut (top_p) or the draw
-// target needs.  A row where that check fails is streamed once more with a
-// lower threshold, and then, if needed, decided by the multi-pass exact
-// selection over the whole row.
+// Sampling in one pass.  While streaming, every lane adds the weight
+// 2^((x - m0) log2e / T) of its raw logits x to its running mass (m0 = the
+// first sub-chunk's maximum), and sets one bit per sub-chunk when its slice
+// holds a logit at or above the row's raw threshold theta (chosen from the
+// first sub-chunk's level counts).  At the end of the row the flagged slices
+// are read again and every unmarked token whose processed score reaches
+// theta_f becomes a candidate; theta_f is chosen so that no token below the
+// raw threshold can reach it.  top_k, the top_p cut and the draw then run
+// exactly on the candidates with fixed-point weights; every other token sits
+// after all candidates in the (score desc, index asc) order, so the result is
+// exact whenever the candidates hold the k largest scores (top_k), or more
+// mass than the cut (top_p) or the draw target needs.  A row where that check
+// fails is read once more with a lower threshold, and then, if needed,
+// decided by the multi-pass exact selection over the whole row.
 #include <mutex>
 
 #include "../../include/tg.h"
@@ -43,12 +49,19 @@ __device__ double* g_dbg = nullptr;
 #endif
 #ifdef TG_DEBUG
 #define TG_GIVEUP(bit) atomicOr(&sm.misc.gcause, (bit))
+__device__ __forceinline__ unsigned long long tg_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// phase timestamps of a row (ns), thread 0 only
+#define TG_T(row, slot) do { if (g_dbg && threadIdx.x == 0) g_dbg[(row) * 16 + 8 + (slot)] = (double)tg_now(); } while (0)
 #else
 #define TG_GIVEUP(bit) do { } while (0)
+#define TG_T(row, slot) do { } while (0)
 #endif
 
-constexpr int kProducerThreads = 32;                 // one producer warp
-constexpr int kSelThreads = kThreads + kProducerThreads;
+constexpr int kMaxRowsPerCta = kThreads;   // rows one CTA owns in one launch (the host splits larger batches)
 
 // ---------------------------------------------------------------------------
 // PTX wrappers: mbarrier + 1-D bulk copy global -> shared
@@ -69,18 +82,13 @@ __device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned
 __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
-                                         unsigned long long* bar, unsigned long long policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ unsigned long long evict_first_policy() {
-  unsigned long long p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
+// 1-D bulk copy global -> shared, completing on `bar`.  No eviction hint:
+// the row stays in L2 for the reads at the end of the row.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
   unsigned ok;
@@ -102,31 +110,26 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned pari
 
 // ---------------------------------------------------------------------------
 // Shared-memory layout of select_kernel:
-//   [SelSmem up to `fin`] [fin | row bitmaps H, N (aliased)] [stage ring]
-// The bitmaps are needed while a row streams; FinSmem only while it is
-// finished; the rare paths that need the bitmaps afterwards rebuild them.
+//   [SelSmem up to `fin`] [fin | row bitmaps M, N (aliased)] [stage ring]
+// The bitmaps are needed until the marked tokens of a row are merged;
+// FinSmem only after that; the rare paths that need the bitmaps afterwards
+// rebuild them.
 // ---------------------------------------------------------------------------
 constexpr int kMaxStages = 8;
-constexpr int kSpecPerWarp = 128;                    // bf16 side list per warp and sub-chunk
 
 struct Misc {
-  unsigned long long full[kMaxStages];   // stage loaded (producer arrive + transaction bytes)
-  unsigned long long empty[kMaxStages];  // stage released (one arrive per consumer warp)
-  int wcnt[kWarps];                      // candidates in each warp's segment
-  float wtheta[kWarps];                  // each warp's threshold at the end of a row
-  float wmref[kWarps];                   // each warp's reference maximum
-  int wflags[kWarps];                    // bit 0: decided, bit 1: gave up
-  int ncand;                             // packed (contiguous) candidates, for the finish
-  int error;                             // a wait timed out; the kernel stops
-  int err_snap;                          // thread 0's snapshot of `error`, read by all consumers
-  int gcause;                            // debug builds: why a warp gave up (bit mask)
-  int issued;                            // sub-chunks the producer has issued (for the error path)
-  float pr_mass[kWarps][32];             // per-warp prune histograms: levels of 0.5 below the max
-  unsigned pr_cnt[kWarps][32];
+  unsigned long long full[kMaxStages];   // stage loaded (one arrive + the copy's transaction bytes)
+  unsigned cnt[kMaxStages];              // warps done with each stage (grows by 16 per use)
+  int iss[kMaxStages];                   // copies issued into each stage
+  int nrow;                              // streamed rows of this CTA
+  int ncand;                             // candidates in the list
+  int error;                             // a wait timed out; the kernel stops loading
+  int err_snap;                          // thread 0's snapshot of `error`, read by all threads
+  int gcause;                            // debug builds: why a row left the one-pass path
+  float wf[kWarps];                      // per-warp scratch
+  unsigned wu[kWarps];
+  unsigned lvl[kWarps][4];               // first sub-chunk: packed counts per level of 2 below m0
 };
-
-// Each warp appends candidates to its own segment of the list (no atomics).
-constexpr int kSeg = kCandCap / kWarps;
 
 constexpr int kLevels = 1024;   // value levels between the lowest candidate and the row max
 constexpr int kGroupCap = 256;  // largest level group sorted exactly in shared memory
@@ -149,8 +152,7 @@ struct FinSmem {
 struct SelSmem {
   float cand_s[kCandCap];
   unsigned cand_i[kCandCap];
-  float spec_s[kWarps * kSpecPerWarp];
-  unsigned spec_i[kWarps * kSpecPerWarp];
+  int rows[kMaxRowsPerCta];   // this CTA's streamed rows, in order
   Hist hist;
   RedScratch red;
   Misc misc;
@@ -215,250 +217,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
-}
-
-// Append one (value, index) per lane that has one to this warp's segment.
-// wc is the warp's count, kept uniform across the warp.
-__device__ __forceinline__ void warp_push(bool has, float v, unsigned i, SelSmem& sm, int& wc) {
-  const unsigned bal = __ballot_sync(0xffffffffu, has);
-  if (bal == 0u) return;
-  const int lane = threadIdx.x & 31;
-  if (has) {
-    const int pos = wc + __popc(bal & ((1u << lane) - 1u));
-    if (pos < kSeg) {
-      const int q = (threadIdx.x >> 5) * kSeg + pos;
-      sm.cand_s[q] = v;
-      sm.cand_i[q] = i;
-    }
-  }
-  wc += __popc(bal);
-}
-
-// Fast mass (relative to c = m * log2e) of this warp's candidates.
-__device__ __forceinline__ float warp_cand_mass(const SelSmem& sm, int wc, float c) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = min(wc, kSeg);
-  float acc = 0.0f;
-  for (int j = lane; j < n; j += 32) acc += wfast(sm.cand_s[w * kSeg + j], c);
-  return warp_sum(acc);
-}
-
-// Drop this warp's candidates below theta (in place); returns the new count
-// and, in `dropped` (all lanes), their fast mass relative to c.
-__device__ __forceinline__ int warp_compact(SelSmem& sm, int wc, float theta, float c, float& dropped) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = min(wc, kSeg);
-  float* S = sm.cand_s + w * kSeg;
-  unsigned* I = sm.cand_i + w * kSeg;
-  int out = 0;
-  float dr = 0.0f;
-  for (int base = 0; base < n; base += 32) {
-    const int j = base + lane;
-    const bool in = j < n;
-    const float s = in ? S[j] : -INFINITY;
-    const unsigned id = in ? I[j] : 0u;
-    const bool keep = in && s >= theta;
-    if (in && !keep) dr += wfast(s, c);
-    const unsigned bal = __ballot_sync(0xffffffffu, keep);
-    __syncwarp();
-    if (keep) {
-      const int pos = out + __popc(bal & ((1u << lane) - 1u));
-      S[pos] = s;
-      I[pos] = id;
-    }
-    out += __popc(bal);
-    __syncwarp();
-  }
-  dropped = warp_sum(dr);
-  return out;
-}
-
-// A higher threshold for this warp's candidates.  top_k: keep at least k of
-// them; otherwise drop at most `allowed` fast mass.  Returns theta' >= theta.
-__device__ float warp_choose_theta(SelSmem& sm, int wc, float theta, float m, float c, bool topk, int k,
-                                   float allowed) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  sm.misc.pr_mass[w][lane] = 0.0f;
-  sm.misc.pr_cnt[w][lane] = 0u;
-  __syncwarp();
-  const int n = min(wc, kSeg);
-  for (int j = lane; j < n; j += 32) {
-    const float s = sm.cand_s[w * kSeg + j];
-    const int lv = static_cast<int>(fminf(fmaxf((m - s) * 2.0f, 0.0f), 31.0f));
-    atomicAdd(&sm.misc.pr_mass[w][lv], wfast(s, c));
-    atomicAdd(&sm.misc.pr_cnt[w][lv], 1u);
-  }
-  __syncwarp();
-  int jstar = 32;
-  if (topk) {
-    unsigned cum = 0u;
-    for (int j = 0; j < 32; ++j) {
-      cum += sm.misc.pr_cnt[w][j];
-      if (cum >= static_cast<unsigned>(k)) { jstar = j + 1; break; }
-    }
-  } else {
-    float tail = 0.0f;
-    for (int j = 31; j >= 0; --j) {
-      const float t2 = tail + sm.misc.pr_mass[w][j];
-      if (t2 > allowed) break;
-      tail = t2;
-      jstar = j;
-    }
-  }
-  __syncwarp();
-  const float cand = (jstar >= 32) ? theta : m - 0.5f * static_cast<float>(jstar);
-  return fmaxf(theta, cand);
-}
-
-// Largest t in [lo, hi] with at least `keep` of this warp's candidates at
-// or above t (bisection on the score; all lanes get the same result).
-__device__ __forceinline__ float warp_keep_score(const SelSmem& sm, int wc, int keep, float lo, float hi) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = min(wc, kSeg);
-  for (int it = 0; it < 20; ++it) {
-    const float mid = 0.5f * (lo + hi);
-    int cnt = 0;
-    for (int j = lane; j < n; j += 32) cnt += sm.cand_s[w * kSeg + j] >= mid ? 1 : 0;
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (cnt >= keep) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// Fast mass of this warp's candidates below t (all lanes).
-__device__ __forceinline__ float warp_mass_below(const SelSmem& sm, int wc, float t, float c) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = min(wc, kSeg);
-  float acc = 0.0f;
-  for (int j = lane; j < n; j += 32) {
-    const float s = sm.cand_s[w * kSeg + j];
-    if (s < t) acc += wfast(s, c);
-  }
-  return warp_sum(acc);
-}
-
-// Make room in this warp's segment: raise theta so that about half of it
-// stays, but never past the point where the excluded mass E (+ what is
-// dropped) exceeds `allowed_frac` of everything this warp has seen; top_k
-// keeps at least k.  Returns the new theta (>= theta).
-__device__ __forceinline__ float warp_make_room(SelSmem& sm, int wc, float theta, float mx, float c, float et_sum,
-                                                bool topk, int k, float allowed_frac) {
-  const int keep = topk ? max(kSeg / 2, k) : kSeg / 2;
-  const float tcap = warp_keep_score(sm, wc, keep, theta, fmaxf(mx, theta));
-  const float zc = warp_cand_mass(sm, wc, c);
-  const float dropped = warp_mass_below(sm, wc, tcap, c);
-  if (topk || et_sum + dropped <= allowed_frac * (et_sum + zc)) return fmaxf(theta, tcap);
-  // the budget stops short of the capacity target: go as far as it allows
-  return warp_choose_theta(sm, wc, theta, mx, c, false, 0, allowed_frac * (et_sum + zc) - et_sum);
-}
-
-// Block-wide choice of a higher threshold over all warps' candidates: top_k
-// keeps at least 2k; otherwise the excluded mass may grow by `allowed`.
-// Every consumer thread calls; all get the same theta' >= theta.
-__device__ float block_choose_theta(SelSmem& sm, int wc, float theta, float m, float c, bool topk, int k,
-                                    float allowed) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  sm.misc.pr_mass[w][lane] = 0.0f;
-  sm.misc.pr_cnt[w][lane] = 0u;
-  __syncwarp();
-  const int n = min(wc, kSeg);
-  for (int j = lane; j < n; j += 32) {
-    const float s = sm.cand_s[w * kSeg + j];
-    const int lv = static_cast<int>(fminf(fmaxf((m - s) * 2.0f, 0.0f), 31.0f));
-    atomicAdd(&sm.misc.pr_mass[w][lv], wfast(s, c));
-    atomicAdd(&sm.misc.pr_cnt[w][lv], 1u);
-  }
-  csync();
-  if (threadIdx.x < 32) {
-    float tm = 0.0f;
-    unsigned tc = 0u;
-    for (int q = 0; q < kWarps; ++q) { tm += sm.misc.pr_mass[q][threadIdx.x]; tc += sm.misc.pr_cnt[q][threadIdx.x]; }
-    sm.misc.pr_mass[0][threadIdx.x] = tm;
-    sm.misc.pr_cnt[0][threadIdx.x] = tc;
-  }
-  csync();
-  int jstar = 32;
-  if (topk) {
-    unsigned cum = 0u;
-    for (int j = 0; j < 32; ++j) {
-      cum += sm.misc.pr_cnt[0][j];
-      if (cum >= static_cast<unsigned>(2 * k)) { jstar = j + 1; break; }
-    }
-  } else {
-    float tail = 0.0f;
-    for (int j = 31; j >= 0; --j) {
-      const float t2 = tail + sm.misc.pr_mass[0][j];
-      if (t2 > allowed) break;
-      tail = t2;
-      jstar = j;
-    }
-  }
-  csync();
-  const float cand = (jstar >= 32) ? theta : m - 0.5f * static_cast<float>(jstar);
-  return fmaxf(theta, cand);
-}
-
-// Block-wide: the lowest threshold theta' >= theta (on levels of 0.5 below
-// m) at which the candidates at or above it, times `scale` (the row's
-// sub-chunks per sub-chunk seen), fill at most three quarters of the list.
-__device__ float block_capacity_theta(SelSmem& sm, int wc, float theta, float m, float scale) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  sm.misc.pr_cnt[w][lane] = 0u;
-  __syncwarp();
-  const int n = min(wc, kSeg);
-  for (int j = lane; j < n; j += 32) {
-    const float s = sm.cand_s[w * kSeg + j];
-    const int lv = static_cast<int>(fminf(fmaxf((m - s) * 2.0f, 0.0f), 31.0f));
-    atomicAdd(&sm.misc.pr_cnt[w][lv], 1u);
-  }
-  csync();
-  if (threadIdx.x < 32) {
-    unsigned tc = 0u;
-    for (int q = 0; q < kWarps; ++q) tc += sm.misc.pr_cnt[q][threadIdx.x];
-    sm.misc.pr_cnt[0][threadIdx.x] = tc;
-  }
-  csync();
-  // level j holds scores in (m - 0.5(j+1), m - 0.5j]; keeping levels < j
-  // means theta' = m - 0.5 j
-  const float cap = 0.75f * static_cast<float>(kCandCap);
-  int jbest = 0;
-  float cum = 0.0f;
-  for (int j = 1; j <= 32; ++j) {
-    cum += static_cast<float>(sm.misc.pr_cnt[0][j - 1]);
-    if (cum * scale <= cap) jbest = j; else break;
-  }
-  csync();
-  const float cand = m - 0.5f * static_cast<float>(jbest);
-  return fmaxf(theta, cand);
-}
-
-// Move the warp segments into one contiguous list [0, ncand).
-__device__ void pack_candidates(SelSmem& sm) {
-  constexpr int kPer = kSeg / 32;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int off = 0;
-  for (int q = 0; q < w; ++q) off += min(sm.misc.wcnt[q], kSeg);
-  const int n = min(sm.misc.wcnt[w], kSeg);
-  float vs[kPer];
-  unsigned is[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int q = lane + 32 * j;
-    vs[j] = q < n ? sm.cand_s[w * kSeg + q] : 0.0f;
-    is[j] = q < n ? sm.cand_i[w * kSeg + q] : 0u;
-  }
-  csync();
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int q = lane + 32 * j;
-    if (q < n) { sm.cand_s[off + q] = vs[j]; sm.cand_i[off + q] = is[j]; }
-  }
-  if (threadIdx.x == 0) {
-    int t = 0;
-    for (int q = 0; q < kWarps; ++q) t += min(sm.misc.wcnt[q], kSeg);
-    sm.misc.ncand = t;
-  }
-  csync();
 }
 
 // ---------------------------------------------------------------------------
@@ -612,9 +370,9 @@ struct FinResult {
   unsigned token;
 };
 
-// top_k, top_p and the draw over the candidates.  E_fix = fixed-point mass
-// of every token below theta.
-__device__ FinResult finalize_candidates(const DevCfg& c, SelSmem& sm, float m, unsigned long long E_fix,
+// top_k, top_p and the draw over the candidates.  Z_all = fixed-point mass
+// of every token of the row (candidates included), relative to m.
+__device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& sm, float m, unsigned long long Z_all,
                                          float u, bool topk, bool topp) {
   const float cc = m * kLog2e;
   const WFast wf{cc};
@@ -674,7 +432,7 @@ __device__ FinResult finalize_candidates(const DevCfg& c, SelSmem& sm, float m, 
     for (int l = threadIdx.x; l < kLevels; l += kThreads) Z += f.lm[l];
     Z = block_sum_u64(Z, &sm.red);
   } else {
-    Z = Zc + E_fix;
+    Z = Z_all > Zc ? Z_all : Zc;
   }
   unsigned long long S = Z;
   int Lc = kLevels;          // level of the cut (kLevels: no cut)
@@ -738,728 +496,678 @@ __device__ FinResult finalize_candidates(const DevCfg& c, SelSmem& sm, float m, 
   return res;
 }
 
-// Select element j (0..N-1) of a register array without dynamic indexing.
+// ---------------------------------------------------------------------------
+// Per-warp slice work.  Warp w owns elements [w*SW, (w+1)*SW) of every
+// sub-chunk (SW = SE / kWarps: 1024 bf16 or 512 f32, i.e. 2 KB).  Lane l
+// holds the slice's 16-byte vectors l, l+32, l+64 and l+96 in registers;
+// element e = i*PER + j of the lane is token tok0 + (lane + 32 i)*PER + j.
+// ---------------------------------------------------------------------------
+struct Slice {
+  uint4 q[4];
+  int nv;    // vectors of the slice inside the row
+};
+
+template <int DT>
+__device__ __forceinline__ void load_slice(const unsigned char* stage, int soff, int scnt, Slice& sl) {
+  constexpr int PER = DT == kF32 ? 4 : 8;
+  const int lane = threadIdx.x & 31;
+  const uint4* v4 = reinterpret_cast<const uint4*>(stage + soff * (DT == kF32 ? 4 : 2));
+  sl.nv = scnt / PER;
+  const unsigned fill = DT == kF32 ? 0xff800000u : 0xff80ff80u;   // -inf
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int v = lane + 32 * i;
+    sl.q[i] = v < sl.nv ? v4[v] : make_uint4(fill, fill, fill, fill);
+  }
+}
+
+// The slice's raw logits as f32 (padding is -inf).
+template <int DT>
+__device__ __forceinline__ void slice_values(const Slice& sl, float (&x)[DT == kF32 ? 16 : 32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const unsigned ps[4] = {sl.q[i].x, sl.q[i].y, sl.q[i].z, sl.q[i].w};
+    if (DT == kF32) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[i * 4 + j] = __uint_as_float(ps[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[i * 8 + j] = (j & 1) ? bf16hi(ps[j >> 1]) : bf16lo(ps[j >> 1]);
+    }
+  }
+}
+
+// Bits of the lane's elements that the bitmap marks (bit e for element e).
+template <int DT>
+__device__ __forceinline__ unsigned slice_marks(const Slice& sl, int tok0, const unsigned* M) {
+  constexpr int PER = DT == kF32 ? 4 : 8;
+  const int lane = threadIdx.x & 31;
+  unsigned mk = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int v = lane + 32 * i;
+    if (v < sl.nv) {
+      const int t = tok0 + v * PER;   // PER divides 32, so the vector's bits share one word
+      mk |= ((M[t >> 5] >> (t & 31)) & ((1u << PER) - 1u)) << (i * PER);
+    }
+  }
+  return mk;
+}
+
+template <int NE>
+__device__ __forceinline__ float tree_max(const float (&x)[NE]) {
+  float t[NE / 2];
+#pragma unroll
+  for (int j = 0; j < NE / 2; ++j) t[j] = fmaxf(x[j], x[j + NE / 2]);
+#pragma unroll
+  for (int w = NE / 4; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+  }
+  return t[0];
+}
+
+// Greedy: the lane's best (score, lowest index) over its unmarked tokens.
+// The lane's tokens increase with e, so only a strictly larger maximum
+// replaces the best, and the lowest e holding it wins.
+template <int DT>
+__device__ __forceinline__ void slice_greedy(const Slice& sl, int tok0, const unsigned* M, bool bitmaps, float& bv,
+                                             unsigned& bi) {
+  constexpr int PER = DT == kF32 ? 4 : 8;
+  constexpr int NE = 4 * PER;
+  const int lane = threadIdx.x & 31;
+  float x[NE];
+  slice_values<DT>(sl, x);
+  if (bitmaps) {
+    const unsigned mk = slice_marks<DT>(sl, tok0, M);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) x[e] = ((mk >> e) & 1u) ? -INFINITY : x[e];
+  }
+  const float vm = tree_max<NE>(x);
+  if (vm > bv) {
+    int ee = NE - 1;
+#pragma unroll
+    for (int e = NE - 2; e >= 0; --e) ee = x[e] == vm ? e : ee;
+    bv = vm;
+    bi = static_cast<unsigned>(tok0 + (lane + 32 * (ee / PER)) * PER + (ee % PER));
+  }
+}
+
+// Error-free sum hi + x = s + e (Knuth's TwoSum); the lane's running mass.
+__device__ __forceinline__ void acc_add(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bb = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+  hi = s;
+  lo = __fadd_rn(lo, e);
+}
+
+// Sampling: the lane's raw weights 2^(x*ascale - cc0) join (ah, al); bit k of
+// emask is set when the lane's slice holds a logit at or above theta_raw.
+template <int DT>
+__device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, float cc0, float theta_raw, int k,
+                                             float& ah, float& al, float& mxt, unsigned& emask) {
+  constexpr int NE = DT == kF32 ? 16 : 32;
+  float x[NE];
+  slice_values<DT>(sl, x);
+  const float vm = tree_max<NE>(x);
+  mxt = fmaxf(mxt, vm);
+  const float2 A = make_float2(ascale, ascale);
+  const float2 C = make_float2(-cc0, -cc0);
+  float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int e = 0; e < NE; e += 2) {
+    float2 w = __ffma2_rn(make_float2(x[e], x[e + 1]), A, C);
+    w.x = ex2_approx(w.x);
+    w.y = ex2_approx(w.y);
+    acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], w);
+  }
+  const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  acc_add(ah, al, t.x + t.y);
+  emask |= (vm >= theta_raw ? 1u : 0u) << k;
+}
+
+// First sub-chunk: per level l = floor((m0 - x) * inv_w), counts of levels
+// 0..7 summed over the warp, as four words of two 16-bit counts
+// (cw[0] = levels 0 and 2, cw[1] = 1 and 3, cw[2] = 4 and 6, cw[3] = 5 and 7).
+template <int DT>
+__device__ __forceinline__ void slice_level_counts(const Slice& sl, float m0, float inv_w, unsigned (&cw)[4]) {
+  constexpr int NE = DT == kF32 ? 16 : 32;
+  float x[NE];
+  slice_values<DT>(sl, x);
+  unsigned lo4 = 0u, hi4 = 0u;   // 8-bit fields: levels 0..3 and 4..7 (at most 32 per lane)
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    const int l = static_cast<int>(fminf((m0 - x[e]) * inv_w, 8.0f));
+    lo4 += l < 4 ? (1u << (8 * l)) : 0u;
+    hi4 += (l >= 4 && l < 8) ? (1u << (8 * (l - 4))) : 0u;
+  }
+  unsigned v[4] = {lo4 & 0x00ff00ffu, (lo4 >> 8) & 0x00ff00ffu, hi4 & 0x00ff00ffu, (hi4 >> 8) & 0x00ff00ffu};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    for (int o = 16; o; o >>= 1) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+    cw[q] = v[q];
+  }
+}
+
+// Element e (0 .. N-1) of a register array, without dynamic indexing.
 template <int N>
-__device__ __forceinline__ float pick(const float (&s)[N], int j) {
+__device__ __forceinline__ float pick_n(const float (&s)[N], int e) {
   float t[N];
 #pragma unroll
   for (int i = 0; i < N; ++i) t[i] = s[i];
 #pragma unroll
   for (int w = N / 2, b = 0; w >= 1; w >>= 1, ++b) {
-    const bool hi = (j >> b) & 1;
+    const bool hi = (e >> b) & 1;
 #pragma unroll
     for (int i = 0; i < w; ++i) t[i] = hi ? t[2 * i + 1] : t[2 * i];
   }
   return t[0];
 }
 
-// ---------------------------------------------------------------------------
-// Per-warp slice work.  Warp w owns elements [w*SW, (w+1)*SW) of every
-// sub-chunk (SW = SE / kWarps: 1024 bf16 or 512 f32, i.e. 2 KB); `soff` is
-// that offset within the stage, `tok0` the slice's first token.
-// ---------------------------------------------------------------------------
+// Append (s, t) to the block's candidate list for every lane with `ok`.
+__device__ __forceinline__ void push_candidate(SelSmem& sm, bool ok, float s, unsigned t) {
+  const int lane = threadIdx.x & 31;
+  const unsigned bal = __ballot_sync(0xffffffffu, ok);
+  if (!bal) return;
+  const int leader = __ffs(bal) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(&sm.misc.ncand, __popc(bal));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (ok) {
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = t; }
+  }
+}
 
-// Patch the tokens the row bitmaps mark in this warp's slice (a2-a9).  f32:
-// the processed score replaces the logit.  bf16: the slot becomes -inf and
-// the exact f32 score goes to the warp's side list; returns its length.
+// End of a sampled row, per warp: read back (from L2) every slice that a
+// lane flagged and append its unmarked tokens with processed score >=
+// theta_f.  Every lane of every warp calls.
 template <int DT>
-__device__ __forceinline__ int warp_patch(unsigned char* stage, int soff, int scnt, int tok0, const unsigned* H,
-                                          const unsigned* N, float rho, float* ss, unsigned* si, bool& ovf) {
-  const int lane = threadIdx.x & 31;
-  const int nw = (scnt + 31) >> 5;
-  unsigned bits = 0u, nb = 0u;
-  if (lane < nw) {
-    const int wd = (tok0 >> 5) + lane;
-    bits = H[wd] | N[wd];
-    nb = N[wd];
-    const int rem = scnt - lane * 32;
-    if (rem < 32) bits &= (1u << rem) - 1u;
-  }
-  int pos = 0, total = 0;
-  if (DT == kBF16) {
-    const int cnt = __popc(bits);
-    int incl = cnt;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    total = __shfl_sync(0xffffffffu, incl, 31);
-    pos = incl - cnt;
-    if (total > kSpecPerWarp) ovf = true;
-  }
-  while (bits) {
-    const int b = __ffs(bits) - 1;
-    bits &= bits - 1u;
-    const int local = soff + lane * 32 + b;
-    if (DT == kF32) {
-      float* sf = reinterpret_cast<float*>(stage);
-      sf[local] = ((nb >> b) & 1u) ? kFilter : penalize(sf[local], rho);
-    } else {
-      unsigned short* sh = reinterpret_cast<unsigned short*>(stage);
-      const float x = __uint_as_float(static_cast<unsigned>(sh[local]) << 16);
-      const float s = ((nb >> b) & 1u) ? kFilter : penalize(x, rho);
-      if (pos < kSpecPerWarp) { ss[pos] = s; si[pos] = static_cast<unsigned>(tok0 + lane * 32 + b); }
-      ++pos;
-      sh[local] = 0xff80u;  // -inf: counted through the side list
-    }
-  }
-  __syncwarp();
-  return DT == kBF16 ? min(total, kSpecPerWarp) : 0;
-}
-
-// Raw (pre-temperature) maximum of this warp's slice, all lanes.
-template <int DT>
-__device__ __forceinline__ float warp_slice_max(const unsigned char* stage, int soff, int scnt, int nspec,
-                                                const float* ss) {
-  const int lane = threadIdx.x & 31;
-  float mx = -INFINITY;
-  if (DT == kF32) {
-    const float4* v4 = reinterpret_cast<const float4*>(stage + soff * 4);
-    const int nv = scnt >> 2;
-    for (int v = lane; v < nv; v += 32) {
-      const float4 q = v4[v];
-      mx = fmaxf(mx, fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w)));
-    }
-    const float* sf = reinterpret_cast<const float*>(stage) + soff;
-    for (int i = (nv << 2) + lane; i < scnt; i += 32) mx = fmaxf(mx, sf[i]);
-  } else {
-    const uint4* v4 = reinterpret_cast<const uint4*>(stage + soff * 2);
-    const int nv = scnt >> 3;
-    __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-    for (int v = lane; v < nv; v += 32) {
-      uint4 q = v4[v];
-      m2 = __hmax2(m2, __hmax2(__hmax2(*reinterpret_cast<__nv_bfloat162*>(&q.x), *reinterpret_cast<__nv_bfloat162*>(&q.y)),
-                               __hmax2(*reinterpret_cast<__nv_bfloat162*>(&q.z), *reinterpret_cast<__nv_bfloat162*>(&q.w))));
-    }
-    mx = fmaxf(__low2float(m2), __high2float(m2));
-    const unsigned short* sh = reinterpret_cast<const unsigned short*>(stage) + soff;
-    for (int i = (nv << 3) + lane; i < scnt; i += 32) mx = fmaxf(mx, __uint_as_float(static_cast<unsigned>(sh[i]) << 16));
-    for (int i = lane; i < nspec; i += 32) mx = fmaxf(mx, ss[i]);
-  }
-  return warp_max(mx);
-}
-
-// Greedy over this warp's slice: each lane keeps its best (score, lowest index).
-template <int DT>
-__device__ __forceinline__ void warp_greedy(const unsigned char* stage, int soff, int scnt, int tok0, int nspec,
-                                            const float* ss, const unsigned* si, float& bv, unsigned& bi) {
-  const int lane = threadIdx.x & 31;
-  if (DT == kF32) {
-    const float4* v4 = reinterpret_cast<const float4*>(stage + soff * 4);
-    const int nv = scnt >> 2;
-    for (int v = lane; v < nv; v += 32) {
-      const float4 q = v4[v];
-      const float vm = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
-      if (vm > bv) {
-        const int j = q.x == vm ? 0 : q.y == vm ? 1 : q.z == vm ? 2 : 3;
-        bv = vm;
-        bi = static_cast<unsigned>(tok0 + 4 * v + j);
-      }
-    }
-    const float* sf = reinterpret_cast<const float*>(stage) + soff;
-    for (int i = (nv << 2) + lane; i < scnt; i += 32)
-      if (sf[i] > bv) { bv = sf[i]; bi = static_cast<unsigned>(tok0 + i); }
-  } else {
-    const uint4* v4 = reinterpret_cast<const uint4*>(stage + soff * 2);
-    const int nv = scnt >> 3;
-    for (int v = lane; v < nv; v += 32) {
-      uint4 q = v4[v];
-      __nv_bfloat162 m2 = __hmax2(__hmax2(*reinterpret_cast<__nv_bfloat162*>(&q.x), *reinterpret_cast<__nv_bfloat162*>(&q.y)),
-                                  __hmax2(*reinterpret_cast<__nv_bfloat162*>(&q.z), *reinterpret_cast<__nv_bfloat162*>(&q.w)));
-      const float vm = fmaxf(__low2float(m2), __high2float(m2));
-      if (vm > bv) {
-        const unsigned ps[4] = {q.x, q.y, q.z, q.w};
-        int jj = 7;
+__device__ void expand_flagged(const DevCfg& c, SelSmem& sm, const unsigned char* rowp, int V, unsigned emask,
+                               const unsigned* M, bool bitmaps, float theta_raw, float theta_f, bool temp_on) {
+  constexpr int esz = DT == kF32 ? 4 : 2;
+  constexpr int PER = DT == kF32 ? 4 : 8;
+  constexpr int NE = 4 * PER;
+  constexpr int SE = kStageBytes / esz;
+  constexpr int SW = SE / kWarps;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  while (__any_sync(0xffffffffu, emask != 0u)) {
+    const bool has = emask != 0u;
+    const int k = has ? __ffs(emask) - 1 : 0;
+    if (has) emask &= emask - 1u;
+    const int lo = k * SE;
+    const int n = min(SE, V - lo);
+    Slice sl;
+    sl.nv = has ? max(0, min(SW, n - wid * SW)) / PER : 0;
+    const int tok0 = lo + wid * SW;
+    const unsigned fill = DT == kF32 ? 0xff800000u : 0xff80ff80u;
 #pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          const float x = (j & 1) ? bf16hi(ps[j >> 1]) : bf16lo(ps[j >> 1]);
-          if (x == vm) jj = j;
-        }
-        bv = vm;
-        bi = static_cast<unsigned>(tok0 + 8 * v + jj);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int v = lane + 32 * i;
+      sl.q[i] = v < sl.nv ? __ldg(reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(tok0 + v * PER) * esz))
+                          : make_uint4(fill, fill, fill, fill);
     }
-    const unsigned short* sh = reinterpret_cast<const unsigned short*>(stage) + soff;
-    for (int i = (nv << 3) + lane; i < scnt; i += 32) {
-      const float x = __uint_as_float(static_cast<unsigned>(sh[i]) << 16);
-      if (x > bv) { bv = x; bi = static_cast<unsigned>(tok0 + i); }
-    }
-    for (int i = lane; i < nspec; i += 32) {
-      const float s = ss[i];
-      const unsigned id = si[i];
-      if (s > bv || (s == bv && id < bi)) { bv = s; bi = id; }
-    }
-  }
-}
-
-// Number of this warp's slice tokens (tempered) at or above t, all lanes.
-template <int DT, bool TEMP>
-__device__ __forceinline__ int warp_slice_count(const unsigned char* stage, int soff, int scnt, int nspec,
-                                                const float* ss, float temp, float t) {
-  const int lane = threadIdx.x & 31;
-  int cnt = 0;
-  for (int i = lane; i < scnt; i += 32) {
-    float s = DT == kF32 ? reinterpret_cast<const float*>(stage)[soff + i]
-                         : __uint_as_float(static_cast<unsigned>(reinterpret_cast<const unsigned short*>(stage)[soff + i]) << 16);
-    if (TEMP) s = temper(s, temp);
-    cnt += s >= t ? 1 : 0;
-  }
-  for (int i = lane; i < nspec; i += 32) cnt += (TEMP ? clampf(__fdiv_rn(ss[i], temp)) : ss[i]) >= t ? 1 : 0;
-  for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  return cnt;
-}
-
-// A slice overflowed the warp's segment: the lowest t (bisection) at which
-// the listed candidates plus the slice's tokens at or above t fill at most
-// three quarters of the segment.
-template <int DT, bool TEMP>
-__device__ float warp_overflow_theta(const SelSmem& sm, int wc, const unsigned char* stage, int soff, int scnt,
-                                     int nspec, const float* ss, float temp, float lo, float hi) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = min(wc, kSeg);
-  const int target = (3 * kSeg) / 4;
-  for (int it = 0; it < 20; ++it) {
-    const float mid = 0.5f * (lo + hi);
-    int cnt = 0;
-    for (int j = lane; j < n; j += 32) cnt += sm.cand_s[w * kSeg + j] >= mid ? 1 : 0;
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    cnt += warp_slice_count<DT, TEMP>(stage, soff, scnt, nspec, ss, temp, mid);
-    if (cnt <= target) hi = mid; else lo = mid;
-  }
-  return hi;
-}
-
-// Sampling over this warp's slice: tokens below theta add their weight
-// 2^(s*log2e - cc) to et, the others go to the warp's candidate segment; mxt
-// tracks the largest (tempered) score.
-template <int DT, bool TEMP>
-__device__ __forceinline__ void warp_pass(const unsigned char* stage, int soff, int scnt, int tok0, int nspec,
-                                          const float* ss, const unsigned* si, SelSmem& sm, float temp, float theta,
-                                          float cc, float& et, float& mxt, int& wc) {
-  constexpr int PER = DT == kF32 ? 4 : 8;      // elements per 16-byte vector
-  constexpr int NE = 2 * PER;                  // elements per lane and round
-  const int lane = threadIdx.x & 31;
-  const int nv = scnt / PER;
-  const unsigned char* base_ptr = stage + soff * (DT == kF32 ? 4 : 2);
-  float* S = sm.cand_s + (threadIdx.x >> 5) * kSeg;
-  unsigned* I = sm.cand_i + (threadIdx.x >> 5) * kSeg;
-  int v0 = 0;
-  // rounds of two vectors per lane: every weight first, then one warp scan
-  for (; v0 + 64 <= nv; v0 += 64) {
-    float s[NE];
-    float vm;
-    const int va = v0 + lane, vb = v0 + 32 + lane;
-    if (DT == kF32) {
-      const float4* v4 = reinterpret_cast<const float4*>(base_ptr);
-      const float4 a = v4[va], b = v4[vb];
-      s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
-      s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
-      vm = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
-    } else {
-      const uint4* v4 = reinterpret_cast<const uint4*>(base_ptr);
-      uint4 a = v4[va], b = v4[vb];
-      const unsigned ps[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int j = 0; j < 16; ++j) s[j] = (j & 1) ? bf16hi(ps[j >> 1]) : bf16lo(ps[j >> 1]);
-      __nv_bfloat162 m2 = __hmax2(__hmax2(__hmax2(*reinterpret_cast<__nv_bfloat162*>(&a.x), *reinterpret_cast<__nv_bfloat162*>(&a.y)),
-                                          __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a.z), *reinterpret_cast<__nv_bfloat162*>(&a.w))),
-                                  __hmax2(__hmax2(*reinterpret_cast<__nv_bfloat162*>(&b.x), *reinterpret_cast<__nv_bfloat162*>(&b.y)),
-                                          __hmax2(*reinterpret_cast<__nv_bfloat162*>(&b.z), *reinterpret_cast<__nv_bfloat162*>(&b.w))));
-      vm = fmaxf(__low2float(m2), __high2float(m2));
-    }
-    if (TEMP) {
-      vm = temper(vm, temp);
-#pragma unroll
-      for (int j = 0; j < NE; ++j) s[j] = temper(s[j], temp);
-    }
-    mxt = fmaxf(mxt, vm);
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float x[NE];
+    slice_values<DT>(sl, x);
     unsigned cm = 0u;
 #pragma unroll
-    for (int j = 0; j < NE; ++j) {
-      const float w = wfast(s[j], cc);
-      const bool cnd = s[j] >= theta;
-      cm |= cnd ? (1u << j) : 0u;
-      acc[j & 3] += cnd ? 0.0f : w;
+    for (int e = 0; e < NE; ++e) cm |= (x[e] >= theta_raw ? 1u : 0u) << e;
+    if (bitmaps) cm &= ~slice_marks<DT>(sl, tok0, M);
+    while (__any_sync(0xffffffffu, cm != 0u)) {
+      const bool h2 = cm != 0u;
+      const int e = h2 ? __ffs(cm) - 1 : 0;
+      if (h2) cm &= cm - 1u;
+      const float xv = pick_n<NE>(x, e);
+      const float s = temp_on ? clampf(__fdiv_rn(xv, c.temp)) : xv;
+      const unsigned t = static_cast<unsigned>(tok0 + (lane + 32 * (e / PER)) * PER + (e % PER));
+      push_candidate(sm, h2 && s >= theta_f, s, t);
     }
-    et += (acc[0] + acc[1]) + (acc[2] + acc[3]);
-    if (__any_sync(0xffffffffu, cm != 0u)) {
-      const int cnt = __popc(cm);
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      int pos = wc + incl - cnt;
-      wc += total;
-      while (cm) {
-        const int j = __ffs(cm) - 1;
-        cm &= cm - 1u;
-        const unsigned id = static_cast<unsigned>(tok0 + (j < PER ? PER * va + j : PER * vb + (j - PER)));
-        if (pos < kSeg) { S[pos] = pick<NE>(s, j); I[pos] = id; }
-        ++pos;
-      }
-    }
-  }
-  // remaining whole vectors, then single elements
-  for (; v0 < nv; v0 += 32) {
-    const int v = v0 + lane;
-    const bool in = v < nv;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      float s = -INFINITY;
-      if (in) {
-        if (DT == kF32) s = reinterpret_cast<const float*>(base_ptr)[v * PER + j];
-        else s = __uint_as_float(static_cast<unsigned>(reinterpret_cast<const unsigned short*>(base_ptr)[v * PER + j]) << 16);
-        if (TEMP) s = temper(s, temp);
-      }
-      mxt = fmaxf(mxt, s);
-      const bool cnd = s >= theta;
-      if (!cnd) et += wfast(s, cc);
-      warp_push(cnd, s, static_cast<unsigned>(tok0 + v * PER + j), sm, wc);
-    }
-  }
-  for (int base = nv * PER; base < scnt; base += 32) {
-    const int i = base + lane;
-    float s = -INFINITY;
-    if (i < scnt) {
-      if (DT == kF32) s = reinterpret_cast<const float*>(base_ptr)[i];
-      else s = __uint_as_float(static_cast<unsigned>(reinterpret_cast<const unsigned short*>(base_ptr)[i]) << 16);
-      if (TEMP) s = temper(s, temp);
-    }
-    mxt = fmaxf(mxt, s);
-    const bool cnd = s >= theta;
-    if (!cnd) et += wfast(s, cc);
-    warp_push(cnd, s, static_cast<unsigned>(tok0 + i), sm, wc);
-  }
-  for (int base = 0; base < nspec; base += 32) {
-    const int i = base + lane;
-    float s = -INFINITY;
-    unsigned id = 0u;
-    if (i < nspec) {
-      s = TEMP ? clampf(__fdiv_rn(ss[i], temp)) : ss[i];
-      id = si[i];
-    }
-    mxt = fmaxf(mxt, s);
-    const bool cnd = s >= theta;
-    if (!cnd) et += wfast(s, cc);
-    warp_push(cnd, s, id, sm, wc);
   }
 }
 
-// Row-wide direct pass from global memory (unaligned rows, the second
-// chance): every token's processed score from the logits and the bitmaps.
-// Greedy: each thread's best.  Sampling with a known theta and cc: tokens
-// below theta add to et, the others join the warp segments (wc).
-template <int DT>
-__device__ void direct_pass(const DevCfg& c, const void* rowp, int V, const unsigned* H, const unsigned* N,
-                            bool bitmaps, bool sample, float theta, float cc, SelSmem& sm, float& bv, unsigned& bi,
-                            float& et, float& mxt, int& wc) {
-  for (int base = 0; base < V; base += kThreads) {
-    const int i = base + threadIdx.x;
-    float s = -INFINITY;
-    if (i < V) {
-      const float x = load_logit<DT>(rowp, i);
-      s = bitmaps ? process_elem(c, H, N, x, i, sample)
-                  : ((sample && c.temp != 1.0f) ? clampf(__fdiv_rn(x, c.temp)) : x);
-    }
-    if (!sample) {
-      if (s > bv) { bv = s; bi = static_cast<unsigned>(i); }
-    } else {
-      mxt = fmaxf(mxt, s);
-      const bool cnd = s >= theta;
-      if (!cnd) et += wfast(s, cc);
-      warp_push(cnd, s, static_cast<unsigned>(i), sm, wc);
+// End of a row: every marked token, read back and processed exactly.
+// Batches of eight per thread keep the reads in flight together.
+template <int DT, class Fn>
+__device__ __forceinline__ void for_marked(const unsigned char* rowp, const unsigned* M, int nwords, Fn fn) {
+  int tb[8];
+  int nb = 0;
+  auto flush = [&]() {
+    float xs[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) xs[q] = q < nb ? load_logit<DT>(rowp, tb[q]) : 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < nb) fn(xs[q], tb[q]);
+    nb = 0;
+  };
+  for (int w = threadIdx.x; w < nwords; w += kThreads) {
+    unsigned bits = M[w];
+    while (bits) {
+      const int t = (w << 5) + __ffs(bits) - 1;
+      bits &= bits - 1u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q == nb) tb[q] = t;
+      if (++nb == 8) flush();
     }
   }
+  flush();
+}
+
+// The candidates could not hold the cut or the draw: read the whole row
+// again (from L2) and take every token at or above a lower threshold.  The
+// row's total mass Z does not change.  Every thread calls.
+template <int DT>
+__device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
+                                                const unsigned char* rowp, unsigned* M, unsigned* N, bool bitmaps,
+                                                float theta_raw, bool tempered, float m, unsigned long long Z,
+                                                float u, bool topk, bool topp) {
+  constexpr int esz = DT == kF32 ? 4 : 2;
+  constexpr int SE = kStageBytes / esz;
+  const int V = a.V;
+  const int nsub = (V + SE - 1) / SE;
+  const float theta_f = tempered ? nextafterf(__fdiv_rn(theta_raw, c.temp), INFINITY) : theta_raw;
+  FinResult res{false, 20, 0u};
+  csync();
+  if (threadIdx.x == 0) sm.misc.ncand = 0;
+  if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords);   // ends with a barrier
+  else csync();
+  const unsigned all = nsub >= 32 ? 0xffffffffu : ((1u << nsub) - 1u);
+  expand_flagged<DT>(c, sm, rowp, V, all, M, bitmaps, theta_raw, theta_f, tempered);
+  if (bitmaps) {
+    for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
+      const float s = process_elem(c, M, N, x, t, true);
+      if (s >= theta_f) {
+        const int pos = atomicAdd(&sm.misc.ncand, 1);
+        if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = static_cast<unsigned>(t); }
+      }
+    });
+  }
+  csync();
+  if (sm.misc.ncand > kCandCap) { res.reason = 24; return res; }
+  return finalize_candidates(c, sm, m, Z, u, topk, topp);
+}
+
+// Multi-pass exact selection over the whole row, read from global memory.
+template <int DT>
+__device__ __noinline__ unsigned slow_select(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
+                                             const unsigned char* rowp, unsigned* H, unsigned* N, bool bitmaps,
+                                             float u) {
+  csync();
+  if (threadIdx.x == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
+  if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords);
+  RowGlobalSource<DT> src{rowp, a.V, &c, H, N, bitmaps, true};
+  float mm = -INFINITY;
+  src.pass([&](float s, unsigned) { mm = fmaxf(mm, s); });
+  mm = block_max(mm, &sm.red);
+  return sample_exact(c, src, mm, u, static_cast<unsigned>(a.V), &sm.hist, &sm.red, nullptr, nullptr);
 }
 
 // ---------------------------------------------------------------------------
 // select_kernel
 // ---------------------------------------------------------------------------
-template <int DT, bool VERIFY, bool TEMP>
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const DevCfg c, const SelArgs a) {
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Forced rows do not depend on the logits: the forced ids score 0, all
+// others the filter value; greedy takes the lowest, sampling draws among them.
+__device__ __forceinline__ int forced_token(const DevCfg& c, const RowMeta& rm, int V, float u, bool sample) {
+  int zs[8];
+  const int nz = forced_zeros(c, rm, zs);
+  if (!sample) return nz ? zs[0] : 0;
+  const unsigned long long W = 1ull << kFixShift;
+  const unsigned long long cnt = nz ? static_cast<unsigned long long>(nz) : static_cast<unsigned long long>(V);
+  unsigned long long ncut = cnt;
+  if (c.top_p < 1.0f) ncut = group_pick(0ull, W, cnt, topp_target(c.top_p, cnt * W), false);
+  const unsigned long long nd = group_pick(0ull, W, ncut, draw_target(u, ncut * W), true);
+  return nz ? zs[nd - 1] : static_cast<int>(nd - 1);
+}
+
+// Block-uniform choice of the sampling threshold from the first sub-chunk's
+// level counts (level l holds tempered scores in (m0 - 2(l+1), m0 - 2l]).
+// Returns l: the threshold is m0 - 2(l+1).  top_k: the first level where the
+// row is expected to hold 4k tokens; otherwise the first level where the mass
+// expected below it is at most a quarter of the (1 - q) the cut or draw
+// allows; never beyond the level where the row's candidates would fill three
+// quarters of the list.  -1: even level 0 would overfill it.
+__device__ __forceinline__ int pilot_level(const unsigned (&cnt)[8], unsigned n_seen, float scale, bool topk,
+                                           int top_k, float qfrac) {
+  const float cap = 0.75f * static_cast<float>(kCandCap);
+  float cum = 0.0f, Z = 0.0f;
+  float wl[8];
+#pragma unroll
+  for (int l = 0; l < 8; ++l) {
+    wl[l] = static_cast<float>(cnt[l]) * __expf(-2.0f * l - 1.0f);
+    Z += wl[l];
+  }
+  unsigned seen = 0u;
+#pragma unroll
+  for (int l = 0; l < 8; ++l) seen += cnt[l];
+  const float rest = static_cast<float>(n_seen - min(seen, n_seen)) * __expf(-17.0f);
+  Z += rest;
+  int jcap = -1, jsel = -1;
+  float below = Z;
+#pragma unroll
+  for (int l = 0; l < 8; ++l) {
+    cum += static_cast<float>(cnt[l]);
+    below -= wl[l];
+    if (cum * scale <= cap) jcap = l;
+    if (jsel < 0) {
+      if (topk ? (cum * scale >= 4.0f * static_cast<float>(top_k)) : (below <= 0.25f * (1.0f - qfrac) * Z)) jsel = l;
+    }
+  }
+  if (jsel < 0) jsel = 7;
+  return jcap < 0 ? -1 : min(jsel, jcap);
+}
+
+template <int DT, bool VERIFY, bool SAMPLE>
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, const SelArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
-  unsigned* H = reinterpret_cast<unsigned*>(smem_raw + fin_offset());
-  unsigned* N = H + bitmap_bytes(a.nwords) / 4;
+  unsigned* M = reinterpret_cast<unsigned*>(smem_raw + fin_offset());   // marked (history | banned)
+  unsigned* N = M + bitmap_bytes(a.nwords) / 4;                         // banned
   unsigned char* ring = smem_raw + ring_offset(a.nwords);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int esz = DT == kF32 ? 4 : 2;
+  constexpr int PER = DT == kF32 ? 4 : 8;
   constexpr int SE = kStageBytes / esz;   // elements per sub-chunk
   constexpr int SW = SE / kWarps;         // elements per warp slice
-  static_assert(SW % 32 == 0 && SW / 32 <= 32, "a warp slice is at most one bitmap word per lane");
+  static_assert(SW == 4 * 32 * PER, "a warp slice is four 16-byte vectors per lane");
   const int V = a.V;
   const int nsub = (V + SE - 1) / SE;
   const int nst = a.nstage;
-  const bool sample = c.mode == kSample;
+  const bool tempered = SAMPLE && c.temp != 1.0f;
   // rows take the TMA ring when every row starts on a 16-byte boundary
   const bool tma_ok = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0u) && ((static_cast<size_t>(V) * esz) % 16u == 0u);
+  const bool bitmaps = !VERIFY && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 ||
+                                   (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
+
+  // Inputs may come from the kernel before this one in the stream.
+  grid_dependency_wait();
 
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
       mbar_init(&sm.misc.full[s], 1u);
-      mbar_init(&sm.misc.empty[s], static_cast<unsigned>(kWarps));
+      sm.misc.cnt[s] = 0u;
+      sm.misc.iss[s] = 0;
     }
     sm.misc.error = 0;
-    sm.misc.issued = 0;
     sm.misc.gcause = 0;
     fence_mbar_init();
   }
-  __syncthreads();
 
-  // ---------------- producer warp: every sub-chunk of every streamed row ----------------
-  if (wid == kWarps) {
-    if (lane == 0) {
-      const unsigned long long policy = evict_first_policy();
-      long long seq = 0;
-      for (int row = blockIdx.x; row < a.nrows && tma_ok; row += gridDim.x) {
-        if (!VERIFY) {
-          const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows);
-          if (rm.bad || rm.L == 0 || rm.forced) continue;
-        }
-        const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
-        for (int k = 0; k < nsub; ++k, ++seq) {
-          const int st = static_cast<int>(seq % nst);
-          const long long use = seq / nst;
-          if (use > 0 && !mbar_wait(&sm.misc.empty[st], static_cast<unsigned>((use - 1) & 1))) {
-            atomicExch(&sm.misc.error, 1);
-            return;
-          }
-          if (*reinterpret_cast<volatile int*>(&sm.misc.error)) return;
-          const int lo = k * SE, n = min(SE, V - lo);
-          mbar_expect_tx(&sm.misc.full[st], static_cast<unsigned>(n * esz));
-          bulk_g2s(ring + st * kStageBytes, rowp + static_cast<size_t>(lo) * esz, static_cast<unsigned>(n * esz),
-                   &sm.misc.full[st], policy);
-          *reinterpret_cast<volatile int*>(&sm.misc.issued) = static_cast<int>(seq + 1);
-        }
+  // ---- this CTA's rows: row_begin + blockIdx.x + i * gridDim.x, one per thread ----
+  const int rel = a.nrows - a.row_begin - static_cast<int>(blockIdx.x);
+  const int nmine = rel > 0 ? min(kMaxRowsPerCta, (rel - 1) / static_cast<int>(gridDim.x) + 1) : 0;
+  bool streamed = false;
+  int myrow = 0;
+  if (tid < nmine) {
+    myrow = a.row_begin + static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x);
+    if (VERIFY) {
+      streamed = true;
+    } else {
+      const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, myrow, a.nrows_total);
+      if (rm.bad || rm.L == 0) {
+        a.out[myrow] = -1;
+        if (rm.bad) atomicOr(c.status, kFlagBadRow);
+      } else if (rm.forced) {
+        const float u = (SAMPLE && a.uniforms) ? a.uniforms[myrow] : 0.0f;
+        a.out[myrow] = forced_token(c, rm, V, u, SAMPLE);
+      } else {
+        streamed = true;
       }
     }
-    return;
   }
+  {
+    // compact the streamed rows, keeping their order
+    const unsigned bal = __ballot_sync(0xffffffffu, streamed);
+    if (lane == 0) sm.misc.wu[wid] = static_cast<unsigned>(__popc(bal));
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int q = 0; q < kWarps; ++q) {
+      const int cq = static_cast<int>(sm.misc.wu[q]);
+      before += q < wid ? cq : 0;
+      total += cq;
+    }
+    if (streamed) sm.rows[before + __popc(bal & ((1u << lane) - 1u))] = myrow;
+    if (tid == 0) sm.misc.nrow = total;
+    __syncthreads();
+  }
+  const int nrow = sm.misc.nrow;
+  const long long total_seq = static_cast<long long>(nrow) * nsub;
 
-  // ---------------- consumer warps ----------------
-  long long seq = 0;
-  for (int row = blockIdx.x; row < a.nrows; row += gridDim.x) {
+  // Load sub-chunk `q` of the schedule (row q / nsub, sub-chunk q % nsub) into its stage.
+  auto issue = [&](long long q) {
+    const int st = static_cast<int>(q % nst);
+    const int row = sm.rows[q / nsub];
+    const int kk = static_cast<int>(q % nsub);
+    const int lo = kk * SE, n = min(SE, V - lo);
+    const unsigned char* src = static_cast<const unsigned char*>(a.logits) + (static_cast<size_t>(row) * V + lo) * esz;
+    mbar_expect_tx(&sm.misc.full[st], static_cast<unsigned>(n * esz));
+    bulk_g2s(ring + st * kStageBytes, src, static_cast<unsigned>(n * esz), &sm.misc.full[st]);
+    sm.misc.iss[st] += 1;
+  };
+  if (tma_ok && tid == 0) {
+    for (long long q = 0; q < nst && q < total_seq; ++q) issue(q);
+  }
+  grid_dependents_launch();
+
+  for (int ri = 0; ri < nrow; ++ri) {
+    const int row = sm.rows[ri];
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
     RowMeta rm;
-    int vb = 0;
     if (VERIFY) {
-      vb = row / (a.K + 1);
       rm.bad = false; rm.L = 1; rm.P = 0; rm.h0 = 0;
       rm.eos_off = rm.forced = rm.forced_eos = rm.bsup = false;
     } else {
-      rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows);
+      rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
     }
-    const float u = (sample && a.uniforms) ? a.uniforms[row] : 0.0f;
-    int token = -1;
+    const float u = (SAMPLE && a.uniforms) ? a.uniforms[row] : 0.0f;
+    const bool topk = SAMPLE && c.top_k > 0 && c.top_k < V;
+    const bool topp = SAMPLE && c.top_p < 1.0f;
+    const float qfrac = topp ? c.top_p : fminf(fmaxf(u, 0.0f), 1.0f);
+    TG_T(row, 0);
+    if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords);
+    TG_T(row, 1);
 
-    if (!VERIFY && (rm.bad || rm.L == 0)) {
-      if (rm.bad && tid == 0) atomicOr(c.status, kFlagBadRow);
-    } else if (!VERIFY && rm.forced) {
-      // Forced rows do not depend on the logits: nothing is read.
-      int zs[8];
-      const int nz = forced_zeros(c, rm, zs);
-      if (!sample) {
-        token = nz ? zs[0] : 0;
-      } else {
-        const unsigned long long W = 1ull << kFixShift;
-        const unsigned long long cnt = nz ? static_cast<unsigned long long>(nz) : static_cast<unsigned long long>(V);
-        unsigned long long ncut = cnt;
-        if (c.top_p < 1.0f) ncut = group_pick(0ull, W, cnt, topp_target(c.top_p, cnt * W), false);
-        const unsigned long long nd = group_pick(0ull, W, ncut, draw_target(u, ncut * W), true);
-        token = nz ? zs[nd - 1] : static_cast<int>(nd - 1);
+    float bv = -INFINITY;            // greedy: this lane's best unmarked score and index
+    unsigned bi = 0xffffffffu;
+    float ah = 0.0f, al = 0.0f;      // sampling: this lane's raw mass relative to cc0 (hi + lo)
+    float mxt = -INFINITY;           // sampling: largest raw logit this lane saw
+    unsigned emask = 0u;             // sampling: sub-chunks where this lane's slice reached theta_raw
+    float theta_raw = INFINITY;      // sampling: raw threshold (block-uniform)
+    float ascale = kLog2e, cc0 = 0.0f;
+    bool decided = false;            // sampling: m0 and theta_raw are set
+
+    if (tma_ok) {
+      for (int k = 0; k < nsub; ++k) {
+        const long long seq = static_cast<long long>(ri) * nsub + k;
+        const int st = static_cast<int>(seq % nst);
+        const unsigned parity = static_cast<unsigned>((seq / nst) & 1);
+        if (!*reinterpret_cast<volatile int*>(&sm.misc.error)) {
+          if (!mbar_wait(&sm.misc.full[st], parity)) atomicExch(&sm.misc.error, 1);
+        }
+        const int lo = k * SE;
+        const int n = min(SE, V - lo);
+        const int scnt = max(0, min(SW, n - wid * SW));
+        const int tok0 = lo + wid * SW;
+        Slice sl;
+        load_slice<DT>(ring + st * kStageBytes, wid * SW, scnt, sl);
+        // the slice is in registers; the sixteenth warp to get here refills the stage
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          const unsigned done = atomicAdd(&sm.misc.cnt[st], 1u);
+          if ((done & (kWarps - 1)) == kWarps - 1) {
+            __threadfence_block();
+            fence_proxy_async();
+            if (seq + nst < total_seq && !*reinterpret_cast<volatile int*>(&sm.misc.error)) issue(seq + nst);
+          }
+        }
+        if (!SAMPLE) {
+          slice_greedy<DT>(sl, tok0, M, bitmaps, bv, bi);
+          continue;
+        }
+        if (k == 0) {
+          // First sub-chunk: the reference maximum m0 and the raw threshold.
+          float mx = -INFINITY;
+          {
+            float x[4 * PER];
+            slice_values<DT>(sl, x);
+            mx = tree_max<4 * PER>(x);
+          }
+          const float m0 = block_max(mx, &sm.red);
+          if (m0 > kFilter && m0 < INFINITY) {
+            const float T = tempered ? c.temp : 1.0f;
+            unsigned cw[4];
+            slice_level_counts<DT>(sl, m0, 0.5f / T, cw);
+            if (lane == 0) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) sm.misc.lvl[wid][q] = cw[q];
+            }
+            csync();
+            unsigned tot[4] = {0u, 0u, 0u, 0u};
+            for (int w = 0; w < kWarps; ++w) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tot[q] += sm.misc.lvl[w][q];
+            }
+            const unsigned cnt[8] = {tot[0] & 0xffffu, tot[1] & 0xffffu, tot[0] >> 16, tot[1] >> 16,
+                                     tot[2] & 0xffffu, tot[3] & 0xffffu, tot[2] >> 16, tot[3] >> 16};
+            const int n0 = min(V, SE);
+            const int jl = pilot_level(cnt, static_cast<unsigned>(n0), static_cast<float>(V) / static_cast<float>(n0),
+                                       topk, c.top_k, qfrac);
+            theta_raw = jl >= 0 ? m0 - 2.0f * T * static_cast<float>(jl + 1) : m0;
+            ascale = tempered ? kLog2e / c.temp : kLog2e;
+            cc0 = m0 * ascale;
+            decided = true;
+          }
+        }
+        if (decided) slice_sample<DT>(sl, ascale, cc0, theta_raw, k, ah, al, mxt, emask);
       }
     } else {
-      const bool bitmaps = !VERIFY;
-      const bool topk = sample && c.top_k > 0 && c.top_k < V;
-      const bool topp = sample && c.top_p < 1.0f;
-      const float qfrac = topp ? c.top_p : fminf(fmaxf(u, 0.0f), 1.0f);
-      const float budget = 0.5f * (1.0f - qfrac);
-      if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords);
-
-      float bv = -INFINITY;          // greedy: this lane's best score and index
-      unsigned bi = 0xffffffffu;
-      float et = 0.0f;               // sampling: this lane's excluded mass, relative to mref
-      float mxt = -INFINITY;         // sampling: largest score this lane saw
-      int wc = 0;                    // this warp's candidates (uniform in the warp)
-      float mref = -INFINITY;        // this warp's reference maximum
-      float cc = 0.0f;               // mref * log2e
-      float theta = -INFINITY;       // this warp's threshold
-      bool decided = false;          // mref and theta are set
-      bool give_up = false;          // the one-pass path cannot decide this row
-      float* ss = sm.spec_s + wid * kSpecPerWarp;
-      unsigned* si = sm.spec_i + wid * kSpecPerWarp;
-
-      if (tma_ok) {
-        for (int k = 0; k < nsub; ++k, ++seq) {
-          const int st = static_cast<int>(seq % nst);
-          const unsigned parity = static_cast<unsigned>((seq / nst) & 1);
-          if (!*reinterpret_cast<volatile int*>(&sm.misc.error)) {
-            if (!mbar_wait(&sm.misc.full[st], parity)) atomicExch(&sm.misc.error, 1);
-          }
-          unsigned char* stage = ring + st * kStageBytes;
-          const int lo = k * SE;
-          const int n = min(SE, V - lo);
-          const int soff = wid * SW;
-          const int scnt = max(0, min(SW, n - soff));
-          const int tok0 = lo + soff;
-          int nspec = 0;
-          if (scnt > 0) {
-            bool sovf = false;
-            if (bitmaps) nspec = warp_patch<DT>(stage, soff, scnt, tok0, H, N, c.rho, ss, si, sovf);
-            if (sovf) { give_up = true; TG_GIVEUP(1); }
-            if (!sample) {
-              warp_greedy<DT>(stage, soff, scnt, tok0, nspec, ss, si, bv, bi);
-            } else if (!give_up) {
-              bool first = false;
-              if (!decided) {
-                float mx = warp_slice_max<DT>(stage, soff, scnt, nspec, ss);
-                if (TEMP) mx = temper(mx, c.temp);
-                if (mx > kFilter) {
-                  mref = mx;
-                  cc = mref * kLog2e;
-                  theta = mref - 8.0f;
-                  decided = true;
-                  first = true;
-                }
-              }
-              if (decided) {
-                bool raised = false;
-                for (int attempt = 0;; ++attempt) {
-                  const float et0 = et, mxt0 = mxt;
-                  const int wc0 = wc;
-                  warp_pass<DT, TEMP>(stage, soff, scnt, tok0, nspec, ss, si, sm, c.temp, theta, cc, et, mxt, wc);
-                  const bool ovf = wc > kSeg;
-                  // (k == 0 is settled block-wide below; later first slices check themselves)
-                  const bool pilot = first && k > 0 && !topk && !raised && attempt < 4;
-                  if (!ovf && !pilot) break;
-                  if (!ovf) {
-                    // first slice: lower theta while too much of its mass lies below it
-                    const float E = warp_sum(et);
-                    const float zc = warp_cand_mass(sm, wc, cc);
-                    if (E <= budget * (E + zc) || theta < mref - 40.0f) break;
-                    et = 0.0f; mxt = mxt0; wc = 0;
-                    theta -= 4.0f;
-                    continue;
-                  }
-                  // overflow: undo the slice, make room, redo
-                  et = et0; mxt = mxt0; wc = wc0;
-                  if (attempt >= 12) { give_up = true; TG_GIVEUP(2); break; }
-                  float hi = fmaxf(mref, warp_max(mxt));
-                  if (TEMP) hi = fmaxf(hi, temper(warp_slice_max<DT>(stage, soff, scnt, nspec, ss), c.temp));
-                  else hi = fmaxf(hi, warp_slice_max<DT>(stage, soff, scnt, nspec, ss));
-                  float th2 = warp_overflow_theta<DT, TEMP>(sm, wc, stage, soff, scnt, nspec, ss, c.temp, theta, hi);
-                  if (topk) th2 = fminf(th2, warp_keep_score(sm, wc, min(wc, c.top_k), theta, hi));
-                  if (!(th2 > theta)) { give_up = true; TG_GIVEUP(4); break; }
-                  if (th2 >= hi) { give_up = true; TG_GIVEUP(8); break; }
-                  theta = th2;
-                  raised = true;
-                  float dropped;
-                  wc = warp_compact(sm, wc, theta, cc, dropped);
-                  if (lane == 0) et += dropped;
-                }
-                // keep a quarter of the segment free
-                if (!give_up && wc > (3 * kSeg) / 4) {
-                  const float th2 = warp_make_room(sm, wc, theta, warp_max(mxt), cc, warp_sum(et), topk, c.top_k,
-                                                   0.9f * (1.0f - qfrac));
-                  if (th2 > theta) {
-                    theta = th2;
-                    float dropped;
-                    wc = warp_compact(sm, wc, theta, cc, dropped);
-                    if (lane == 0) et += dropped;
-                  }
-                }
-              }
-            }
-          }
-          // First sub-chunk: one block-wide decision of theta from all sixteen
-          // slices (its stage is kept until then, so it can be redone).
-          if (sample && k == 0) {
-            for (int round = 0;; ++round) {
-              csync();
-              if (lane == 0) {
-                sm.misc.wmref[wid] = mref;
-                sm.misc.wflags[wid] = (decided ? 1 : 0) | (give_up ? 2 : 0);
-              }
-              csync();
-              float m0 = -INFINITY;
-              bool any_gu = false;
-              for (int q = 0; q < kWarps; ++q) {
-                const int fl = sm.misc.wflags[q];
-                if (fl & 1) m0 = fmaxf(m0, sm.misc.wmref[q]);
-                any_gu |= (fl & 2) != 0;
-              }
-              if (any_gu || !(m0 > kFilter)) break;   // each warp goes on by itself
-              // one reference maximum and one threshold for every warp
-              const float cc0 = m0 * kLog2e;
-              et = decided ? et * expf(mref - m0) : 0.0f;
-              if (!decided) { wc = 0; mxt = -INFINITY; }
-              mref = m0;
-              cc = cc0;
-              decided = true;
-              const float th0 = round == 0 ? m0 - 8.0f : theta;
-              float dropped;
-              wc = warp_compact(sm, wc, th0, cc, dropped);
-              if (lane == 0) et += dropped;
-              theta = th0;
-              // project the first sub-chunk over the whole row
-              const float scale = static_cast<float>(V) / static_cast<float>(min(V, SE));
-              const float E = block_sum_f(et, &sm.red);
-              const float zcw = warp_cand_mass(sm, wc, cc);
-              const float zc = block_sum_f(lane == 0 ? zcw : 0.0f, &sm.red);
-              const float nct = block_sum_f(lane == 0 ? static_cast<float>(min(wc, kSeg)) : 0.0f, &sm.red);
-              if (!topk && E * scale > 0.5f * (1.0f - qfrac) * (E + zc) && nct * scale < 0.5f * kCandCap &&
-                  round < 3 && theta > m0 - 40.0f) {
-                // too much mass below theta and room to spare: lower it, redo the sub-chunk
-                theta -= 2.0f;
-                et = 0.0f; mxt = -INFINITY; wc = 0;
-                if (scnt > 0) {
-                  warp_pass<DT, TEMP>(stage, soff, scnt, tok0, nspec, ss, si, sm, c.temp, theta, cc, et, mxt, wc);
-                  if (wc > kSeg) give_up = true;
-                }
-                continue;
-              }
-              // as low a threshold as the list's capacity allows
-              const float th1 = block_capacity_theta(sm, wc, theta, m0, scale);
-              if (th1 > theta) {
-                theta = th1;
-                wc = warp_compact(sm, wc, theta, cc, dropped);
-                if (lane == 0) et += dropped;
-              }
-              break;
-            }
-          }
-          // release the stage to the producer
-          if (bitmaps) fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.misc.empty[st]);
-        }
-      } else {
-        // rows not on a 16-byte boundary: read the logits directly
-        if (!sample) {
-          float et_unused = 0.0f, mxt_unused = -INFINITY;
-          int wc_unused = 0;
-          direct_pass<DT>(c, rowp, V, H, N, bitmaps, false, 0.0f, 0.0f, sm, bv, bi, et_unused, mxt_unused, wc_unused);
-        } else {
-          float mx = -INFINITY;
-          for (int i = tid; i < V; i += kThreads) {
-            const float x = load_logit<DT>(rowp, i);
-            mx = fmaxf(mx, bitmaps ? process_elem(c, H, N, x, i, true)
-                                   : ((c.temp != 1.0f) ? clampf(__fdiv_rn(x, c.temp)) : x));
-          }
-          mx = block_max(mx, &sm.red);
-          if (mx > kFilter) {
-            mref = mx;
-            cc = mref * kLog2e;
-            theta = mref - 8.0f;
-            decided = true;
-            direct_pass<DT>(c, rowp, V, H, N, bitmaps, true, theta, cc, sm, bv, bi, et, mxt, wc);
-            if (wc > kSeg) give_up = true;
-          }
+      // rows not on a 16-byte boundary: read the logits directly
+      if (!SAMPLE) {
+        for (int i = tid; i < V; i += kThreads) {
+          if (bitmaps && get_bit(M, i)) continue;
+          const float x = load_logit<DT>(rowp, i);
+          if (x > bv) { bv = x; bi = static_cast<unsigned>(i); }
         }
       }
+    }
 
-      // ---------------- finish the row (all consumer warps) ----------------
-      csync();
+    // ---------------- finish the row (all threads) ----------------
+    TG_T(row, 2);
+    int token = -1;
+    if (!SAMPLE) {
+      // marked tokens, processed exactly, against the best unmarked one
+      if (bitmaps) {
+        for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
+          const float s = process_elem(c, M, N, x, t, false);
+          if (s > bv || (s == bv && static_cast<unsigned>(t) < bi)) { bv = s; bi = static_cast<unsigned>(t); }
+        });
+      }
+      for (int o = 16; o; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const unsigned i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (v2 > bv || (v2 == bv && i2 < bi)) { bv = v2; bi = i2; }
+      }
+      if (lane == 0) { sm.misc.wf[wid] = bv; sm.misc.wu[wid] = bi; }
       if (tid == 0) sm.misc.err_snap = *reinterpret_cast<volatile int*>(&sm.misc.error);
       csync();
-      if (sm.misc.err_snap) break;   // uniform: every consumer reads the same snapshot
-      if (!sample) {
-        const float m = block_max(bv, &sm.red);
-        token = static_cast<int>(block_min_u(bv == m ? bi : 0xffffffffu, &sm.red));
-      } else {
-        if (lane == 0) {
-          sm.misc.wtheta[wid] = theta;
-          sm.misc.wmref[wid] = mref;
-          sm.misc.wflags[wid] = (decided ? 1 : 0) | ((give_up || wc > kSeg) ? 2 : 0);
-          if (wc > kSeg) TG_GIVEUP(16);
+      if (sm.misc.err_snap) break;   // uniform: every thread reads the same snapshot
+      if (tid == 0) {
+        float v = sm.misc.wf[0];
+        unsigned b = sm.misc.wu[0];
+        for (int q = 1; q < kWarps; ++q) {
+          const float v2 = sm.misc.wf[q];
+          const unsigned i2 = sm.misc.wu[q];
+          if (v2 > v || (v2 == v && i2 < b)) { v = v2; b = i2; }
         }
-        csync();
-        bool any_give_up = false, any_decided = false;
-        float theta_f = -INFINITY, mref_max = -INFINITY;
-        for (int q = 0; q < kWarps; ++q) {
-          const int fl = sm.misc.wflags[q];
-          any_give_up |= (fl & 2) != 0;
-          if (fl & 1) {
-            any_decided = true;
-            theta_f = fmaxf(theta_f, sm.misc.wtheta[q]);
-            mref_max = fmaxf(mref_max, sm.misc.wmref[q]);
-          }
+        token = static_cast<int>(b);
+      }
+    } else {
+      const float wmx = warp_max(mxt);
+      if (lane == 0) sm.misc.wf[wid] = wmx;
+      if (tid == 0) {
+        sm.misc.err_snap = *reinterpret_cast<volatile int*>(&sm.misc.error);
+        sm.misc.ncand = 0;
+      }
+      csync();
+      if (sm.misc.err_snap) break;
+      float m_raw = -INFINITY;
+      for (int q = 0; q < kWarps; ++q) m_raw = fmaxf(m_raw, sm.misc.wf[q]);
+      bool slow = !decided || !tma_ok || !(m_raw > kFilter);
+      int reason = slow ? 3 : 0;
+      unsigned tok = 0u;
+      const float T = tempered ? c.temp : 1.0f;
+      // every unmarked token with a processed score >= theta_f has x >= theta_raw
+      const float theta_f = tempered ? nextafterf(__fdiv_rn(theta_raw, T), INFINITY) : theta_raw;
+      const float m = tempered ? clampf(__fdiv_rn(m_raw, T)) : m_raw;   // >= every unmarked score
+      const float cc_m = m * kLog2e;
+      if (!slow) {
+        expand_flagged<DT>(c, sm, rowp, V, emask, M, bitmaps, theta_raw, theta_f, tempered);
+        TG_T(row, 3);
+        // the hot mass counted marked tokens at their raw weight: swap in the processed one
+        float wr = 0.0f, wp = 0.0f;
+        bool over = false;
+        if (bitmaps) {
+          for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
+            const float s = process_elem(c, M, N, x, t, true);
+            wr += ex2_approx(fmaf(x, ascale, -cc0));
+            wp += wfast(s, cc_m);
+            over |= s > m;
+            if (s >= theta_f) {
+              const int pos = atomicAdd(&sm.misc.ncand, 1);
+              if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = static_cast<unsigned>(t); }
+            }
+          });
         }
-        const float m = fmaxf(mref_max, block_max(mxt, &sm.red));
-        bool slow = any_give_up || !any_decided || !(m > kFilter);
-        int reason = any_give_up ? 1 : slow ? 3 : 0;
-        unsigned tok = 0u;
-        const float cc_m = m * kLog2e;
+        const float f0 = ex2_approx(cc0 - cc_m);   // cc0 - cc_m <= 0: m0 <= m_raw
+        const float hot = ah + al;
+        const double zl = (static_cast<double>(hot) - static_cast<double>(wr)) * f0 + static_cast<double>(wp);
+        const unsigned long long zq = static_cast<unsigned long long>(llrint(zl * kFixScale));
+        const unsigned long long Zs = block_sum_u64(zq, &sm.red);   // two's complement: exact signed sum
+        const float hot_sum = block_sum_f(hot, &sm.red);
+        const float wr_sum = block_sum_f(wr, &sm.red);
+        const int any_over = __syncthreads_or(over ? 1 : 0);
+        const long long Zsigned = static_cast<long long>(Zs);
+        if (any_over || wr_sum > 0.5f * hot_sum || Zsigned <= 0) { slow = true; reason = 2; }
+        const int ncand = sm.misc.ncand;
+        if (!slow && ncand > kCandCap) { slow = true; reason = 4; }
+        TG_DBG(row, 2, m); TG_DBG(row, 3, theta_f); TG_DBG(row, 4, static_cast<double>(Zsigned) / kFixScale);
+        TG_DBG(row, 7, ncand);
+        TG_T(row, 4);
         if (!slow) {
-          // every warp drops its candidates below the largest theta
-          et = decided ? et * expf(mref - m) : 0.0f;
-          float dropped;
-          wc = warp_compact(sm, wc, theta_f, cc_m, dropped);
-          if (lane == 0) { et += dropped; sm.misc.wcnt[wid] = wc; }
-          const float E = block_sum_f(et, &sm.red);
-          pack_candidates(sm);
-          TG_DBG(row, 2, m); TG_DBG(row, 3, theta_f); TG_DBG(row, 4, E); TG_DBG(row, 7, sm.misc.ncand);
-          const FinResult fr = finalize_candidates(
-              c, sm, m, static_cast<unsigned long long>(llrint(static_cast<double>(E) * kFixScale)), u, topk, topp);
+          const FinResult fr = finalize_candidates(c, sm, m, static_cast<unsigned long long>(Zsigned), u, topk, topp);
           slow = !fr.ok;
           if (slow) reason = fr.reason;
           tok = fr.token;
           // Too little candidate mass for the cut or draw: one more pass, read
           // directly (the row is likely still in L2), with a lower threshold.
           if (slow && (reason == 5 || reason == 7)) {
-            csync();
-            if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords);
-            float et2 = 0.0f, mxt2 = -INFINITY;
-            int wc2 = 0;
-            float bv2 = -INFINITY;
-            unsigned bi2 = 0u;
-            direct_pass<DT>(c, rowp, V, H, N, bitmaps, true, theta_f - 1.5f, cc_m, sm, bv2, bi2, et2, mxt2, wc2);
-            if (lane == 0) sm.misc.wflags[wid] = wc2 > kSeg ? 2 : 0;
-            csync();
-            bool ovf2 = false;
-            for (int q = 0; q < kWarps; ++q) ovf2 |= (sm.misc.wflags[q] & 2) != 0;
-            if (!ovf2) {
-              if (lane == 0) sm.misc.wcnt[wid] = wc2;
-              const float E2 = block_sum_f(et2, &sm.red);
-              pack_candidates(sm);
-              const FinResult fr2 = finalize_candidates(
-                  c, sm, m, static_cast<unsigned long long>(llrint(static_cast<double>(E2) * kFixScale)), u, topk, topp);
-              slow = !fr2.ok;
-              if (slow) reason = 10 + fr2.reason;
-              tok = fr2.token;
-            }
+            TG_T(row, 5);
+            const FinResult fr2 = second_chance<DT>(c, a, sm, rm, rowp, M, N, bitmaps, theta_raw - 2.0f * T, tempered, m,
+                                                    static_cast<unsigned long long>(Zsigned), u, topk, topp);
+            slow = !fr2.ok;
+            if (slow) reason = 10 + fr2.reason;
+            tok = fr2.token;
           }
         }
-        TG_DBG(row, 0, slow ? 1 : 0); TG_DBG(row, 1, reason);
-#ifdef TG_DEBUG
-        TG_DBG(row, 5, sm.misc.gcause);
-        csync();
-        if (tid == 0) sm.misc.gcause = 0;
-#endif
-        if (slow) {
-          // Multi-pass exact selection over the whole row.
-          csync();
-          if (tid == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
-          if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords);
-          RowGlobalSource<DT> src{rowp, V, &c, H, N, bitmaps, true};
-          float mm = -INFINITY;
-          src.pass([&](float s, unsigned) { mm = fmaxf(mm, s); });
-          mm = block_max(mm, &sm.red);
-          tok = sample_exact(c, src, mm, u, static_cast<unsigned>(V), &sm.hist, &sm.red, nullptr, nullptr);
-        }
-        token = static_cast<int>(tok);
       }
+      TG_DBG(row, 0, slow ? 1 : 0); TG_DBG(row, 1, reason);
+      TG_T(row, 6);
+      if (slow) tok = slow_select<DT>(c, a, sm, rm, rowp, M, N, bitmaps, u);
+      token = static_cast<int>(tok);
     }
 
     // ---------------- outputs ----------------
+    TG_T(row, 7);
     if (tid == 0) {
       a.out[row] = token;
       if (VERIFY) {
         // Last of the K+1 positions of row vb counts the matches (steps 4-5).
+        const int vb = row / (a.K + 1);
         __threadfence();
         const unsigned prev = atomicAdd(&c.tickets[vb], 1u);
         if (prev == static_cast<unsigned>(a.K)) {
@@ -1477,14 +1185,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const DevCfg c, 
     csync();
   }
 
-  // error: wait (bounded) for every copy the producer issued, then leave
-  if (*reinterpret_cast<volatile int*>(&sm.misc.error)) {
-    if (tid == 0) {
-      atomicOr(c.status, kFlagTimeout);
-      for (int tries = 0; tries < 4 * kMaxStages && seq < *reinterpret_cast<volatile int*>(&sm.misc.issued); ++tries, ++seq) {
-        const int st = static_cast<int>(seq % nst);
-        mbar_wait(&sm.misc.full[st], static_cast<unsigned>((seq / nst) & 1));
-      }
+  // error: wait (bounded) for the copies still in flight, then leave
+  __syncthreads();
+  if (sm.misc.error && tid == 0) {
+    atomicOr(c.status, kFlagTimeout);
+    for (int s = 0; s < nst; ++s) {
+      const int n = sm.misc.iss[s];
+      if (n > 0) mbar_wait(&sm.misc.full[s], static_cast<unsigned>((n - 1) & 1));
     }
   }
 }
@@ -1687,6 +1394,7 @@ extern "C" tg_status tg_verify_noalloc(const void* target_logits, int32_t B, int
   memset(&a, 0, sizeof(a));
   a.logits = target_logits;
   a.nrows = B * (K + 1);
+  a.nrows_total = a.nrows;
   a.V = V;
   a.uniforms = uniforms;
   a.out = out_next;
@@ -1707,25 +1415,44 @@ int process_smem_bytes(int nwords) {
   return align_up(static_cast<int>(sizeof(ProcSmem)), 128) + 2 * bitmap_bytes(nwords);
 }
 
-template <int DT, bool VERIFY, bool TEMP>
+// One launch per kMaxRowsPerCta * grid rows; each is a programmatic dependent
+// of the kernel before it in the stream (its launch overlaps that kernel's
+// tail; it waits for it before touching global memory).
+template <int DT, bool VERIFY, bool SAMPLE>
 static cudaError_t launch_sel(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s) {
-  auto k = select_kernel<DT, VERIFY, TEMP>;
+  auto k = select_kernel<DT, VERIFY, SAMPLE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kSelThreads, smem, s>>>(c, a);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const long long per_launch = static_cast<long long>(grid) * kMaxRowsPerCta;
+  for (long long r0 = 0; r0 < a.nrows_total; r0 += per_launch) {
+    SelArgs b = a;
+    b.row_begin = static_cast<int>(r0);
+    b.nrows = static_cast<int>(r0 + per_launch < a.nrows_total ? r0 + per_launch : a.nrows_total);
+    e = cudaLaunchKernelEx(&cfg, k, c, b);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
 template <int DT, bool VERIFY>
-static cudaError_t launch_sel_t(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s) {
-  const bool temp = c.mode == kSample && c.temp != 1.0f;
-  return temp ? launch_sel<DT, VERIFY, true>(c, a, grid, smem, s) : launch_sel<DT, VERIFY, false>(c, a, grid, smem, s);
+static cudaError_t launch_sel_m(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s) {
+  return c.mode == kSample ? launch_sel<DT, VERIFY, true>(c, a, grid, smem, s) : launch_sel<DT, VERIFY, false>(c, a, grid, smem, s);
 }
 
 cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s) {
-  if (a.nstage < 2 || a.nstage > kMaxStages) return cudaErrorInvalidValue;
-  if (c.dtype == kF32) return verify ? launch_sel_t<kF32, true>(c, a, grid, smem, s) : launch_sel_t<kF32, false>(c, a, grid, smem, s);
-  return verify ? launch_sel_t<kBF16, true>(c, a, grid, smem, s) : launch_sel_t<kBF16, false>(c, a, grid, smem, s);
+  if (a.nstage < 2 || a.nstage > kMaxStages || grid < 1) return cudaErrorInvalidValue;
+  if (c.dtype == kF32) return verify ? launch_sel_m<kF32, true>(c, a, grid, smem, s) : launch_sel_m<kF32, false>(c, a, grid, smem, s);
+  return verify ? launch_sel_m<kBF16, true>(c, a, grid, smem, s) : launch_sel_m<kBF16, false>(c, a, grid, smem, s);
 }
 
 cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
@@ -1755,7 +1482,7 @@ cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_s
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kSelThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, smem);
     if (e != cudaSuccess) return e;
     worst = occ < worst ? occ : worst;
   }
