@@ -122,6 +122,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // Fast weight used only for the excluded mass: 2^(s*log2e - m*log2e).
 __device__ __forceinline__ float wfast(float s, float c) { return ex2_approx(fmaf(s, kLog2e, -c)); }
 
+// round(x * 2^44) for a finite x in [0, 2^19), ties to even: the value
+// __float2ull_rn(x * 2^44) gives, computed with integer operations only (a
+// 64-bit float-to-integer conversion is a slow instruction on this GPU).
+__device__ __forceinline__ unsigned long long fix44(float x) {
+  const unsigned b = __float_as_uint(x);
+  const int e = static_cast<int>((b >> 23) & 0xffu);
+  if (e == 0 || (b >> 31)) return 0ull;            // zero, subnormal (< 2^-126) or negative
+  if (e >= 127 + 19) return 0x7fffffffffffffffull; // out of range (or inf/nan): saturate
+  const unsigned long long mant = static_cast<unsigned long long>((b & 0x7fffffu) | 0x800000u);
+  const int sh = e - 127 - 23 + kFixShift;          // x * 2^44 = mant * 2^sh
+  if (sh >= 0) return mant << sh;
+  const int r = -sh;
+  if (r > 24) return 0ull;                           // below one half
+  const unsigned long long q = mant >> r;
+  const unsigned long long rem = mant & ((1ull << r) - 1ull);
+  const unsigned long long half = 1ull << (r - 1);
+  return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
+}
+
 // Accurate weight exp(s - m) in fixed point (x 2^44).  s - m is formed
 // exactly as hi + lo (TwoSum); exp(hi + lo) ~= exp(hi) * (1 + lo).
 __device__ __forceinline__ unsigned long long wfix(float s, float m) {
@@ -132,13 +151,13 @@ __device__ __forceinline__ unsigned long long wfix(float s, float m) {
   float e = expf(hi);
   float w = fmaf(e, lo, e);
   w = fminf(fmaxf(w, 0.0f), 1.0f);
-  return __float2ull_rn(w * 17592186044416.0f);
+  return fix44(w);
 }
 
 // Fast weight in fixed point: the one-pass path's weight, consistent with
 // the excluded mass it accumulates with wfast (cc = m * log2e).
 __device__ __forceinline__ unsigned long long wfix_fast(float s, float cc) {
-  return __float2ull_rn(wfast(s, cc) * 17592186044416.0f);
+  return fix44(wfast(s, cc));
 }
 
 // Weight functors for the radix engine.
@@ -411,18 +430,44 @@ __device__ __forceinline__ unsigned long long group_pick(unsigned long long abov
   return n;
 }
 
+// p * Z for a float p in [0, 1] and a 64-bit Z, exactly: p = mant * 2^-k
+// with a 24-bit mant, so p * Z = (mant * Z) / 2^k with a 128-bit numerator.
+// Returns floor(p * Z) and whether p * Z is not an integer.
+__device__ __forceinline__ unsigned long long mul_frac(float p, unsigned long long Z, bool* inexact) {
+  const unsigned b = __float_as_uint(p);
+  const int e = static_cast<int>((b >> 23) & 0xffu);
+  *inexact = false;
+  if (e == 0 || (b >> 31) || Z == 0ull) { *inexact = false; return 0ull; }
+  const unsigned long long mant = static_cast<unsigned long long>((b & 0x7fffffu) | 0x800000u);
+  const int k = 150 - e;                       // p = mant * 2^-k
+  const unsigned long long lo = mant * Z, hi = __umul64hi(mant, Z);
+  if (k <= 0) return lo << (-k);               // p >= 2^23: not reached for p <= 1
+  if (k >= 128) { *inexact = (lo | hi) != 0ull; return 0ull; }
+  unsigned long long q, rem_nonzero;
+  if (k >= 64) {
+    q = k == 64 ? hi : hi >> (k - 64);
+    rem_nonzero = lo | (k == 64 ? 0ull : (hi & ((1ull << (k - 64)) - 1ull)));
+  } else {
+    q = (lo >> k) | (hi << (64 - k));
+    rem_nonzero = lo & ((1ull << k) - 1ull);
+  }
+  *inexact = rem_nonzero != 0ull;
+  return q;
+}
+
 // Mass target of the top-p cut: the smallest integer >= p * Z.
 __device__ __forceinline__ unsigned long long topp_target(float p, unsigned long long Z) {
-  double t = static_cast<double>(p) * static_cast<double>(Z);
-  unsigned long long T = static_cast<unsigned long long>(ceil(t));
+  bool inexact;
+  const unsigned long long f = mul_frac(p, Z, &inexact);
+  const unsigned long long T = f + (inexact ? 1ull : 0ull);
   return T > Z ? Z : T;
 }
 // Mass target of the draw: the largest integer <= u * S, u in [0, 1).
 __device__ __forceinline__ unsigned long long draw_target(float u, unsigned long long S) {
   if (!(u >= 0.0f)) u = 0.0f;               // NaN or negative -> 0
   if (u >= 1.0f) u = 0x1.fffffep-1f;        // largest float below 1
-  double t = static_cast<double>(u) * static_cast<double>(S);
-  unsigned long long T = static_cast<unsigned long long>(floor(t));
+  bool inexact;
+  const unsigned long long T = mul_frac(u, S, &inexact);
   return (T >= S && S > 0) ? S - 1 : T;
 }
 

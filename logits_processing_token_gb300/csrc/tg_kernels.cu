@@ -43,25 +43,24 @@ namespace tg {
 #ifdef TG_DEBUG
 // Debug builds only: per-row record {path, reason, m, theta, E, Zc, Z, ncand}.
 __device__ double* g_dbg = nullptr;
-#define TG_DBG(row, slot, val) do { if (g_dbg && threadIdx.x == 0) g_dbg[(row) * 16 + (slot)] = (double)(val); } while (0)
+#define TG_DBG(row, slot, val) do { if (g_dbg && threadIdx.x == 0) g_dbg[(row) * 32 + (slot)] = (double)(val); } while (0)
 #else
 #define TG_DBG(row, slot, val) do { } while (0)
 #endif
 #ifdef TG_DEBUG
 #define TG_GIVEUP(bit) atomicOr(&sm.misc.gcause, (bit))
-__device__ __forceinline__ unsigned long long tg_now() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-// phase timestamps of a row (ns), thread 0 only
-#define TG_T(row, slot) do { if (g_dbg && threadIdx.x == 0) g_dbg[(row) * 16 + 8 + (slot)] = (double)tg_now(); } while (0)
+__device__ __forceinline__ unsigned long long tg_now() { return clock64(); }
+// phase timestamps of a row (SM cycles), thread 0 only
+#define TG_T(row, slot) do { if (g_dbg && threadIdx.x == 0) g_dbg[(row) * 32 + 8 + (slot)] = (double)tg_now(); } while (0)
+#define TG_TF(slot) TG_T(sm.misc.dbg_row, slot)
 #else
+#define TG_TF(slot) do { } while (0)
 #define TG_GIVEUP(bit) do { } while (0)
 #define TG_T(row, slot) do { } while (0)
 #endif
 
 constexpr int kMaxRowsPerCta = kThreads;   // rows one CTA owns in one launch (the host splits larger batches)
+constexpr int kEvCap = 4096;               // flagged units a row may list
 
 // ---------------------------------------------------------------------------
 // PTX wrappers: mbarrier + 1-D bulk copy global -> shared
@@ -126,6 +125,7 @@ struct Misc {
   int error;                             // a wait timed out; the kernel stops loading
   int err_snap;                          // thread 0's snapshot of `error`, read by all threads
   int gcause;                            // debug builds: why a row left the one-pass path
+  int dbg_row;                           // debug builds: the row being finished
   float wf[kWarps];                      // per-warp scratch
   unsigned wu[kWarps];
   unsigned lvl[kWarps][4];               // first sub-chunk: packed counts per level of 2 below m0
@@ -137,22 +137,26 @@ constexpr int kGroupCap = 256;  // largest level group sorted exactly in shared 
 struct FinSmem {
   unsigned long long lm[kLevels];  // weight of each level
   unsigned lc[kLevels];            // items in each level
+  unsigned lw[3][kLevels];         // the weights in three 15-bit limbs (exact sums with 32-bit atomics)
   unsigned gk[kGroupCap];          // gathered group: key, index, weight
   unsigned gi[kGroupCap];
   unsigned long long gw[kGroupCap];
   unsigned sk[kGroupCap];          // the group sorted by (key desc, index asc)
   unsigned si[kGroupCap];
   unsigned long long sw[kGroupCap];
+  unsigned long long wsum[kWarps]; // per-warp partial sums of a block scan
   int gn;
   int fb;                          // broadcast: bucket / position
   unsigned long long fbefore;      // broadcast: mass or count before it
   int ffound;
+  int lastne;                      // last non-empty level (a search that finds nothing)
 };
 
 struct SelSmem {
   float cand_s[kCandCap];
   unsigned cand_i[kCandCap];
   int rows[kMaxRowsPerCta];   // this CTA's streamed rows, in order
+  unsigned short ev[kEvCap];   // flagged units of the row being finished
   Hist hist;
   RedScratch red;
   Misc misc;
@@ -300,60 +304,92 @@ __device__ int gather_sort_level(SelSmem& sm, int n, const LevelMap& lv, int lev
 
 // One warp: the first sorted position j < cnt where base + sum(sw[0..j])
 // reaches the target (>= or >).  Writes fin.fb = j (or cnt-1 when never),
-// fin.fbefore = base + sum(sw[0..j-1]), fin.ffound.
+// fin.fbefore = base + sum(sw[0..j-1]), fin.ffound.  The warp scans 32
+// positions at a time (lane = position within the chunk).
 __device__ __forceinline__ void walk_sorted(SelSmem& sm, int cnt, unsigned long long base,
                                             unsigned long long target, bool strict) {
   FinSmem& f = sm.fin;
   if (threadIdx.x < 32) {
-    constexpr int PER = kGroupCap / 32;
     const int lane = threadIdx.x;
-    unsigned long long local = 0ull;
-    for (int j = 0; j < PER; ++j) {
-      const int q = lane * PER + j;
-      if (q < cnt) local += f.sw[q];
-    }
-    unsigned long long incl = local;
-    for (int o = 1; o < 32; o <<= 1) {
-      unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned long long excl = incl - local;
-    const unsigned long long tot = base + incl;
-    const unsigned hit = __ballot_sync(0xffffffffu, strict ? tot > target : tot >= target);
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      if (lane == L) {
-        unsigned long long cum = base + excl;
-        int j = lane * PER;
-        for (; j < lane * PER + PER && j < cnt; ++j) {
-          const unsigned long long nx = cum + f.sw[j];
-          if (strict ? nx > target : nx >= target) break;
-          cum = nx;
-        }
-        f.fb = j;
-        f.fbefore = cum;
-        f.ffound = 1;
+    unsigned long long run = base;
+    bool done = false;
+    for (int c0 = 0; c0 < cnt && !done; c0 += 32) {
+      const int q = c0 + lane;
+      const unsigned long long w = q < cnt ? f.sw[q] : 0ull;
+      unsigned long long incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
       }
-    } else if (lane == 0) {
-      unsigned long long all = 0ull;
+      const unsigned long long tot = run + incl;
+      const unsigned hit = __ballot_sync(0xffffffffu, q < cnt && (strict ? tot > target : tot >= target));
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        if (lane == L) {
+          f.fb = q;
+          f.fbefore = tot - w;
+          f.ffound = 1;
+        }
+        done = true;
+      } else {
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (!done && lane == 0) {
+      unsigned long long all = base;
       for (int j = 0; j + 1 < cnt; ++j) all += f.sw[j];
       f.fb = cnt - 1;
-      f.fbefore = base + all;
+      f.fbefore = all;
       f.ffound = 0;
     }
   }
   csync();
 }
 
-// Level search by warp 0 over fin.lm / fin.lc; results in fin.fb/fbefore/ffound.
-template <class Reached>
-__device__ __forceinline__ void level_find_mass(SelSmem& sm, Reached r) {
-  if (threadIdx.x < 32) {
-    FindOut<unsigned long long> o = warp_find<kLevels>(sm.fin.lm, sm.fin.lc, false, r);
-    if (threadIdx.x == 0) { sm.fin.fb = o.b; sm.fin.fbefore = o.before; sm.fin.ffound = o.found; }
+// Block-wide search over the levels: the first level l where the running
+// sum of fin.lm reaches the target (Reached); fin.fb = l, fin.fbefore = the
+// sum of the levels before l, fin.ffound = 1.  When no level reaches it:
+// fin.fb = the last non-empty level, fin.fbefore = the sum before it,
+// fin.ffound = 0.  Every thread calls; thread t owns levels 2t and 2t+1.
+template <class T, class Reached>
+__device__ __forceinline__ void level_find(SelSmem& sm, const T* vals, Reached r) {
+  static_assert(kLevels == 2 * kThreads, "two levels per thread");
+  FinSmem& f = sm.fin;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned long long v0 = vals[2 * tid], v1 = vals[2 * tid + 1];
+  const bool ne0 = f.lc[2 * tid] != 0u, ne1 = f.lc[2 * tid + 1] != 0u;
+  const unsigned long long local = v0 + v1;
+  unsigned long long incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
+  if (lane == 31) f.wsum[wid] = incl;
+  if (tid == 0) { f.ffound = 0; f.lastne = -1; }
   csync();
+  unsigned long long before = 0ull;
+  for (int q = 0; q < wid; ++q) before += f.wsum[q];
+  const unsigned long long excl = before + incl - local;
+  if (r(excl + local) && (tid == 0 || !r(excl))) {
+    if (r(excl + v0)) { f.fb = 2 * tid; f.fbefore = excl; }
+    else { f.fb = 2 * tid + 1; f.fbefore = excl + v0; }
+    f.ffound = 1;
+  }
+  if (ne0 || ne1) atomicMax(&f.lastne, ne1 ? 2 * tid + 1 : 2 * tid);
+  csync();
+  if (!f.ffound) {
+    const int L = f.lastne;
+    if (L >= 0 && (L >> 1) == tid) {
+      f.fb = L;
+      f.fbefore = (L & 1) ? excl + v0 : excl;
+    }
+    csync();
+  }
 }
+template <class Reached>
+__device__ __forceinline__ void level_find_mass(SelSmem& sm, Reached r) { level_find(sm, sm.fin.lm, r); }
 
 // Keep only levels < L in full and the first `mass`/`cnt` of level L.
 __device__ __forceinline__ void level_limit(SelSmem& sm, int L, unsigned long long mass, unsigned cnt) {
@@ -372,43 +408,44 @@ struct FinResult {
 
 // top_k, top_p and the draw over the candidates.  Z_all = fixed-point mass
 // of every token of the row (candidates included), relative to m.
-__device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& sm, float m, unsigned long long Z_all,
-                                         float u, bool topk, bool topp) {
+__device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& sm, float m, float lo,
+                                                      unsigned long long Z_all, float u, bool topk, bool topp) {
   const float cc = m * kLog2e;
   const WFast wf{cc};
   FinResult res{false, 0, 0u};
   FinSmem& f = sm.fin;
   const int n = min(sm.misc.ncand, kCandCap);
   if (n <= 0) { res.reason = 9; return res; }
-  // level map from the lowest candidate to the maximum
-  float smin = INFINITY;
-  for (int i = threadIdx.x; i < n; i += kThreads) smin = fminf(smin, sm.cand_s[i]);
-  smin = -block_max(-smin, &sm.red);
-  const float range = m - smin;
+  // level map from the threshold (every candidate is at or above it) to the maximum
+  TG_TF(8);
+  const float range = m - lo;
   LevelMap lv{m, range > 0.0f ? static_cast<float>(kLevels - 1) / range : 0.0f};
-  for (int l = threadIdx.x; l < kLevels; l += kThreads) { f.lm[l] = 0ull; f.lc[l] = 0u; }
+  for (int l = threadIdx.x; l < kLevels; l += kThreads) { f.lc[l] = 0u; f.lw[0][l] = 0u; f.lw[1][l] = 0u; f.lw[2][l] = 0u; }
   csync();
   unsigned long long zc = 0ull;
   for (int i = threadIdx.x; i < n; i += kThreads) {
     const float s = sm.cand_s[i];
     const int l = lv(s);
-    const unsigned long long w = wfix_fast(s, cc);
+    const unsigned long long w = wfix_fast(s, cc);   // <= 2^44
     zc += w;
-    atomicAdd(&f.lm[l], w);
     atomicAdd(&f.lc[l], 1u);
+    atomicAdd(&f.lw[0][l], static_cast<unsigned>(w & 0x7fffull));
+    atomicAdd(&f.lw[1][l], static_cast<unsigned>((w >> 15) & 0x7fffull));
+    atomicAdd(&f.lw[2][l], static_cast<unsigned>(w >> 30));
   }
+  csync();
+  for (int l = threadIdx.x; l < kLevels; l += kThreads)
+    f.lm[l] = static_cast<unsigned long long>(f.lw[0][l]) + (static_cast<unsigned long long>(f.lw[1][l]) << 15) +
+              (static_cast<unsigned long long>(f.lw[2][l]) << 30);
   const unsigned long long Zc = block_sum_u64(zc, &sm.red);
+  TG_TF(9);
   unsigned klo = 0u;
   unsigned long long Z;
   if (topk) {
     if (n < c.top_k) { res.reason = 4; return res; }
     // level holding the k-th largest token
-    if (threadIdx.x < 32) {
-      const unsigned need = static_cast<unsigned>(c.top_k);
-      FindOut<unsigned> o = warp_find<kLevels>(f.lc, f.lc, false, [need](unsigned x) { return x >= need; });
-      if (threadIdx.x == 0) { f.fb = o.b; f.fbefore = o.before; }
-    }
-    csync();
+    const unsigned long long need = static_cast<unsigned long long>(c.top_k);
+    level_find(sm, f.lc, [need](unsigned long long x) { return x >= need; });
     const int Lk = f.fb;
     const unsigned rank = static_cast<unsigned>(c.top_k) - static_cast<unsigned>(f.fbefore);
     const int gn = gather_sort_level(sm, n, lv, Lk, 0u, cc);
@@ -443,11 +480,13 @@ __device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& 
     const unsigned long long T = topp_target(c.top_p, Z);
     if (!topk && Zc < T) { res.reason = 5; return res; }
     level_find_mass(sm, [T](unsigned long long x) { return x >= T; });
+    TG_TF(10);
     if (!f.ffound) { res.reason = 6; return res; }
     Lc = f.fb;
     const unsigned long long before = f.fbefore;
     csync();
     const int gn = gather_sort_level(sm, n, lv, Lc, klo, cc);
+    TG_TF(11);
     unsigned long long inlevel;
     if (gn >= 0) {
       walk_sorted(sm, gn, before, T, false);
@@ -467,10 +506,12 @@ __device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& 
     }
     csync();
     level_limit(sm, Lc, inlevel, static_cast<unsigned>(nc));
+    TG_TF(12);
   }
   const unsigned long long Td = draw_target(u, S);
   if (!topk && !topp && !(Zc > Td)) { res.reason = 7; return res; }
   level_find_mass(sm, [Td](unsigned long long x) { return x > Td; });
+  TG_TF(13);
   if (!f.ffound) { res.reason = 8; return res; }
   const int Ld = f.fb;
   const unsigned long long before = f.fbefore;
@@ -492,6 +533,7 @@ __device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& 
     }
   }
   csync();
+  TG_TF(14);
   res.ok = true;
   return res;
 }
@@ -602,15 +644,39 @@ __device__ __forceinline__ void acc_add(float& hi, float& lo, float x) {
   lo = __fadd_rn(lo, e);
 }
 
-// Sampling: the lane's raw weights 2^(x*ascale - cc0) join (ah, al); bit k of
-// emask is set when the lane's slice holds a logit at or above theta_raw.
+// Units of eight elements: a lane's slice holds four (bf16: one vector each)
+// or two (f32: vectors i and i+1 of the lane).  Unit u covers elements
+// 8u .. 8u+7 of the lane's slice.
+template <int DT>
+struct Units {
+  static constexpr int kPerSlice = DT == kF32 ? 2 : 4;
+};
+
+// Sampling: the lane's raw weights 2^(x*ascale - cc0) join (ah, al); bit
+// k*UPS + u of emask is set when unit u of the lane's slice in sub-chunk k
+// holds a logit at or above theta_raw.
 template <int DT>
 __device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, float cc0, float theta_raw, int k,
-                                             float& ah, float& al, float& mxt, unsigned& emask) {
+                                             float& ah, float& al, float& mxt, unsigned long long& emask) {
   constexpr int NE = DT == kF32 ? 16 : 32;
+  constexpr int UPS = Units<DT>::kPerSlice;
   float x[NE];
   slice_values<DT>(sl, x);
-  const float vm = tree_max<NE>(x);
+  float um[UPS];
+#pragma unroll
+  for (int u = 0; u < UPS; ++u) {
+    float t[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) t[j] = fmaxf(x[8 * u + j], x[8 * u + j + 4]);
+    um[u] = fmaxf(fmaxf(t[0], t[2]), fmaxf(t[1], t[3]));
+  }
+  float vm = um[0];
+  unsigned bits = um[0] >= theta_raw ? 1u : 0u;
+#pragma unroll
+  for (int u = 1; u < UPS; ++u) {
+    vm = fmaxf(vm, um[u]);
+    bits |= (um[u] >= theta_raw ? 1u : 0u) << u;
+  }
   mxt = fmaxf(mxt, vm);
   const float2 A = make_float2(ascale, ascale);
   const float2 C = make_float2(-cc0, -cc0);
@@ -624,7 +690,7 @@ __device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, floa
   }
   const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
   acc_add(ah, al, t.x + t.y);
-  emask |= (vm >= theta_raw ? 1u : 0u) << k;
+  emask |= static_cast<unsigned long long>(bits) << (k * UPS);
 }
 
 // First sub-chunk: per level l = floor((m0 - x) * inv_w), counts of levels
@@ -680,48 +746,193 @@ __device__ __forceinline__ void push_candidate(SelSmem& sm, bool ok, float s, un
   }
 }
 
-// End of a sampled row, per warp: read back (from L2) every slice that a
-// lane flagged and append its unmarked tokens with processed score >=
-// theta_f.  Every lane of every warp calls.
+// Append (s, t) for every set bit e of cm (s = sv[e], t = tok[e]) to the
+// block's candidate list: one reservation per warp, then each lane writes
+// its own.  Every lane of the warp calls.
+__device__ __forceinline__ void push_units(SelSmem& sm, unsigned cm, const float (&sv)[8], const unsigned (&tok)[8]) {
+  const int lane = threadIdx.x & 31;
+  const int cnt = __popc(cm);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total == 0) return;
+  int base = 0;
+  if (lane == 31) base = atomicAdd(&sm.misc.ncand, total);
+  base = __shfl_sync(0xffffffffu, base, 31);
+  int pos = base + incl - cnt;
+  while (cm) {
+    const int e = __ffs(cm) - 1;
+    cm &= cm - 1u;
+    if (pos < kCandCap) {
+      float v = sv[0];
+      unsigned ti = tok[0];
+#pragma unroll
+      for (int q = 1; q < 8; ++q) {
+        v = e == q ? sv[q] : v;
+        ti = e == q ? tok[q] : ti;
+      }
+      sm.cand_s[pos] = v;
+      sm.cand_i[pos] = ti;
+    }
+    ++pos;
+  }
+}
+
+// End of a sampled row: the units that lanes flagged while streaming, as one
+// list for the block (entry = k << 11 | warp << 7 | lane << 2 | unit).
+// Returns the number of flagged units (the list holds at most kEvCap).
 template <int DT>
-__device__ void expand_flagged(const DevCfg& c, SelSmem& sm, const unsigned char* rowp, int V, unsigned emask,
-                               const unsigned* M, bool bitmaps, float theta_raw, float theta_f, bool temp_on) {
+__device__ __forceinline__ int list_flagged(SelSmem& sm, unsigned long long emask) {
+  constexpr int UPS = Units<DT>::kPerSlice;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int cnt = __popcll(emask);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm.misc.wu[wid] = static_cast<unsigned>(incl);
+  csync();
+  int base = 0, total = 0;
+  for (int q = 0; q < kWarps; ++q) {
+    const int cq = static_cast<int>(sm.misc.wu[q]);
+    base += q < wid ? cq : 0;
+    total += cq;
+  }
+  int pos = base + incl - cnt;
+  while (emask) {
+    const int b = __ffsll(static_cast<long long>(emask)) - 1;
+    emask &= emask - 1ull;
+    if (pos < kEvCap)
+      sm.ev[pos] = static_cast<unsigned short>(((b / UPS) << 11) | (wid << 7) | (lane << 2) | (b % UPS));
+    ++pos;
+  }
+  csync();
+  return total;
+}
+
+// Read units back (from L2), eight logits each, and append every unmarked
+// token whose processed score reaches theta_f (its raw logit is at or above
+// theta_raw).  The units are the listed ones (nev of them), or with `every`
+// all units of the row.  Thread t takes entries t, t + kThreads, ...; a batch
+// issues all of its reads first, then reserves room for all of its
+// candidates with one warp-wide reservation.  Every thread calls.
+template <int DT>
+__device__ void expand_units(const DevCfg& c, SelSmem& sm, const unsigned char* rowp, int V, int nev, bool every,
+                             const unsigned* M, bool bitmaps, float theta_raw, float theta_f, bool temp_on) {
   constexpr int esz = DT == kF32 ? 4 : 2;
   constexpr int PER = DT == kF32 ? 4 : 8;
-  constexpr int NE = 4 * PER;
   constexpr int SE = kStageBytes / esz;
   constexpr int SW = SE / kWarps;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  while (__any_sync(0xffffffffu, emask != 0u)) {
-    const bool has = emask != 0u;
-    const int k = has ? __ffs(emask) - 1 : 0;
-    if (has) emask &= emask - 1u;
-    const int lo = k * SE;
-    const int n = min(SE, V - lo);
-    Slice sl;
-    sl.nv = has ? max(0, min(SW, n - wid * SW)) / PER : 0;
-    const int tok0 = lo + wid * SW;
-    const unsigned fill = DT == kF32 ? 0xff800000u : 0xff80ff80u;
+  constexpr int UPS = Units<DT>::kPerSlice;
+  constexpr int NQ = DT == kF32 ? 2 : 1;    // 16-byte vectors per unit
+  constexpr int B = DT == kF32 ? 4 : 8;     // entries per thread per batch (B * 8 candidate bits <= 64)
+  const int lane = threadIdx.x & 31;
+  const int nsub = (V + SE - 1) / SE;
+  const int n = every ? (nsub << 11) : min(nev, kEvCap);
+  const unsigned fill = DT == kF32 ? 0xff800000u : 0xff80ff80u;
+  for (int j0 = 0; j0 < n; j0 += B * kThreads) {
+    const int nb = min(B, (n - j0 + kThreads - 1) / kThreads);   // uniform
+    uint4 q[B][NQ];
+    int t0[B];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int v = lane + 32 * i;
-      sl.q[i] = v < sl.nv ? __ldg(reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(tok0 + v * PER) * esz))
-                          : make_uint4(fill, fill, fill, fill);
+    for (int b = 0; b < B; ++b) {
+      t0[b] = -1;
+#pragma unroll
+      for (int h = 0; h < NQ; ++h) q[b][h] = make_uint4(fill, fill, fill, fill);
+      const int j = j0 + b * kThreads + static_cast<int>(threadIdx.x);
+      if (b < nb && j < n) {
+        const unsigned en = every ? static_cast<unsigned>(j) : sm.ev[j];
+        const int kk = static_cast<int>(en >> 11), w = static_cast<int>((en >> 7) & 15u);
+        const int ln = static_cast<int>((en >> 2) & 31u), uu = static_cast<int>(en & 3u);
+        const int nv = max(0, min(SW, min(SE, V - kk * SE) - w * SW)) / PER;   // vectors inside the row
+        const int base = kk * SE + w * SW;
+        const int v0 = ln + 32 * (NQ * uu);
+        if (uu < UPS && v0 < nv) {
+          t0[b] = base + v0 * PER;
+#pragma unroll
+          for (int h = 0; h < NQ; ++h)
+            if (v0 + 32 * h < nv)
+              q[b][h] = __ldg(reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(base + (v0 + 32 * h) * PER) * esz));
+        }
+      }
     }
-    float x[NE];
-    slice_values<DT>(sl, x);
-    unsigned cm = 0u;
+    unsigned long long cmall = 0ull;
 #pragma unroll
-    for (int e = 0; e < NE; ++e) cm |= (x[e] >= theta_raw ? 1u : 0u) << e;
-    if (bitmaps) cm &= ~slice_marks<DT>(sl, tok0, M);
-    while (__any_sync(0xffffffffu, cm != 0u)) {
-      const bool h2 = cm != 0u;
-      const int e = h2 ? __ffs(cm) - 1 : 0;
-      if (h2) cm &= cm - 1u;
-      const float xv = pick_n<NE>(x, e);
-      const float s = temp_on ? clampf(__fdiv_rn(xv, c.temp)) : xv;
-      const unsigned t = static_cast<unsigned>(tok0 + (lane + 32 * (e / PER)) * PER + (e % PER));
-      push_candidate(sm, h2 && s >= theta_f, s, t);
+    for (int b = 0; b < B; ++b) {
+      if (b < nb && t0[b] >= 0) {
+        float x[8];
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+          const unsigned ps[4] = {q[b][h].x, q[b][h].y, q[b][h].z, q[b][h].w};
+#pragma unroll
+          for (int e = 0; e < 8 / NQ; ++e)
+            x[h * (8 / NQ) + e] = DT == kF32 ? __uint_as_float(ps[e]) : ((e & 1) ? bf16hi(ps[e >> 1]) : bf16lo(ps[e >> 1]));
+        }
+        unsigned cm = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm |= (x[e] >= theta_raw ? 1u : 0u) << e;
+        if (bitmaps && cm) {
+          unsigned mk;
+          if (DT == kF32) {
+            const int a0 = t0[b], a1 = t0[b] + 32 * PER;
+            mk = (M[a0 >> 5] >> (a0 & 31)) & 15u;
+            if (cm >> 4) mk |= ((M[a1 >> 5] >> (a1 & 31)) & 15u) << 4;
+          } else {
+            mk = (M[t0[b] >> 5] >> (t0[b] & 31)) & 255u;
+          }
+          cm &= ~mk;
+        }
+        if (temp_on && cm) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if ((cm >> e) & 1u) x[e] = clampf(__fdiv_rn(x[e], c.temp));
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm &= ~((x[e] >= theta_f ? 0u : 1u) << e);
+        cmall |= static_cast<unsigned long long>(cm) << (8 * b);
+      }
+    }
+    // one reservation per warp for all of this batch's candidates
+    const int cnt = __popcll(cmall);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) continue;
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sm.misc.ncand, total);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int pos = base + incl - cnt;
+    while (cmall) {
+      const int bit = __ffsll(static_cast<long long>(cmall)) - 1;
+      cmall &= cmall - 1ull;
+      const int b = bit >> 3, e = bit & 7;
+      const int h = e / (8 / NQ), ee = e % (8 / NQ);
+      uint4 v = q[0][0];
+      int tb = t0[0];
+#pragma unroll
+      for (int bb = 0; bb < B; ++bb)
+#pragma unroll
+        for (int hh = 0; hh < NQ; ++hh)
+          if (bb == b && hh == h) { v = q[bb][hh]; tb = t0[bb]; }
+      const unsigned wsel = (ee >> (DT == kF32 ? 0 : 1)) == 0 ? v.x : (ee >> (DT == kF32 ? 0 : 1)) == 1 ? v.y
+                          : (ee >> (DT == kF32 ? 0 : 1)) == 2 ? v.z : v.w;
+      float xv = DT == kF32 ? __uint_as_float(wsel) : ((ee & 1) ? bf16hi(wsel) : bf16lo(wsel));
+      if (temp_on) xv = clampf(__fdiv_rn(xv, c.temp));
+      if (pos < kCandCap) {
+        sm.cand_s[pos] = xv;
+        sm.cand_i[pos] = static_cast<unsigned>(tb + h * 32 * PER + ee);
+      }
+      ++pos;
     }
   }
 }
@@ -763,18 +974,14 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
                                                 const unsigned char* rowp, unsigned* M, unsigned* N, bool bitmaps,
                                                 float theta_raw, bool tempered, float m, unsigned long long Z,
                                                 float u, bool topk, bool topp) {
-  constexpr int esz = DT == kF32 ? 4 : 2;
-  constexpr int SE = kStageBytes / esz;
   const int V = a.V;
-  const int nsub = (V + SE - 1) / SE;
   const float theta_f = tempered ? nextafterf(__fdiv_rn(theta_raw, c.temp), INFINITY) : theta_raw;
   FinResult res{false, 20, 0u};
   csync();
   if (threadIdx.x == 0) sm.misc.ncand = 0;
   if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords);   // ends with a barrier
   else csync();
-  const unsigned all = nsub >= 32 ? 0xffffffffu : ((1u << nsub) - 1u);
-  expand_flagged<DT>(c, sm, rowp, V, all, M, bitmaps, theta_raw, theta_f, tempered);
+  expand_units<DT>(c, sm, rowp, V, 0, true, M, bitmaps, theta_raw, theta_f, tempered);
   if (bitmaps) {
     for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
       const float s = process_elem(c, M, N, x, t, true);
@@ -786,7 +993,7 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
   }
   csync();
   if (sm.misc.ncand > kCandCap) { res.reason = 24; return res; }
-  return finalize_candidates(c, sm, m, Z, u, topk, topp);
+  return finalize_candidates(c, sm, m, theta_f, Z, u, topk, topp);
 }
 
 // Multi-pass exact selection over the whole row, read from global memory.
@@ -859,6 +1066,41 @@ __device__ __forceinline__ int pilot_level(const unsigned (&cnt)[8], unsigned n_
   }
   if (jsel < 0) jsel = 7;
   return jcap < 0 ? -1 : min(jsel, jcap);
+}
+
+// One barrier for all of a sampled row's sums: the exact fixed-point mass
+// (two's complement, so signed parts add up exactly), the raw streaming mass,
+// the raw mass of the marked tokens, and whether any processed score exceeded
+// the reference maximum.  Every thread calls; all get the totals.
+struct RowSums {
+  unsigned long long z;
+  float hot, wr;
+  bool over;
+};
+__device__ __forceinline__ RowSums block_row_sums(SelSmem& sm, unsigned long long z, float hot, float wr, bool over) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int o = 16; o; o >>= 1) {
+    z += __shfl_xor_sync(0xffffffffu, z, o);
+    hot += __shfl_xor_sync(0xffffffffu, hot, o);
+    wr += __shfl_xor_sync(0xffffffffu, wr, o);
+  }
+  const bool ov = __any_sync(0xffffffffu, over);
+  csync();
+  if (lane == 0) {
+    sm.red.q[wid] = z;
+    sm.red.f[wid] = hot;
+    sm.red.u[wid] = __float_as_uint(wr);
+    sm.misc.wu[wid] = ov ? 1u : 0u;
+  }
+  csync();
+  RowSums r{0ull, 0.0f, 0.0f, false};
+  for (int q = 0; q < kWarps; ++q) {
+    r.z += sm.red.q[q];
+    r.hot += sm.red.f[q];
+    r.wr += __uint_as_float(sm.red.u[q]);
+    r.over |= sm.misc.wu[q] != 0u;
+  }
+  return r;
 }
 
 template <int DT, bool VERIFY, bool SAMPLE>
@@ -967,6 +1209,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     const bool topk = SAMPLE && c.top_k > 0 && c.top_k < V;
     const bool topp = SAMPLE && c.top_p < 1.0f;
     const float qfrac = topp ? c.top_p : fminf(fmaxf(u, 0.0f), 1.0f);
+#ifdef TG_DEBUG
+    if (tid == 0) sm.misc.dbg_row = row;
+#endif
     TG_T(row, 0);
     if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords);
     TG_T(row, 1);
@@ -975,7 +1220,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     unsigned bi = 0xffffffffu;
     float ah = 0.0f, al = 0.0f;      // sampling: this lane's raw mass relative to cc0 (hi + lo)
     float mxt = -INFINITY;           // sampling: largest raw logit this lane saw
-    unsigned emask = 0u;             // sampling: sub-chunks where this lane's slice reached theta_raw
+    unsigned long long emask = 0ull; // sampling: units (sub-chunk, unit) of this lane that reached theta_raw
     float theta_raw = INFINITY;      // sampling: raw threshold (block-uniform)
     float ascale = kLog2e, cc0 = 0.0f;
     bool decided = false;            // sampling: m0 and theta_raw are set
@@ -1094,6 +1339,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         sm.misc.ncand = 0;
       }
       csync();
+      TG_T(row, 15);
       if (sm.misc.err_snap) break;
       float m_raw = -INFINITY;
       for (int q = 0; q < kWarps; ++q) m_raw = fmaxf(m_raw, sm.misc.wf[q]);
@@ -1106,7 +1352,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       const float m = tempered ? clampf(__fdiv_rn(m_raw, T)) : m_raw;   // >= every unmarked score
       const float cc_m = m * kLog2e;
       if (!slow) {
-        expand_flagged<DT>(c, sm, rowp, V, emask, M, bitmaps, theta_raw, theta_f, tempered);
+        const int nev = list_flagged<DT>(sm, emask);
+        TG_T(row, 16);
+        expand_units<DT>(c, sm, rowp, V, nev, false, M, bitmaps, theta_raw, theta_f, tempered);
+        TG_T(row, 17);
         TG_T(row, 3);
         // the hot mass counted marked tokens at their raw weight: swap in the processed one
         float wr = 0.0f, wp = 0.0f;
@@ -1125,21 +1374,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         }
         const float f0 = ex2_approx(cc0 - cc_m);   // cc0 - cc_m <= 0: m0 <= m_raw
         const float hot = ah + al;
-        const double zl = (static_cast<double>(hot) - static_cast<double>(wr)) * f0 + static_cast<double>(wp);
-        const unsigned long long zq = static_cast<unsigned long long>(llrint(zl * kFixScale));
-        const unsigned long long Zs = block_sum_u64(zq, &sm.red);   // two's complement: exact signed sum
-        const float hot_sum = block_sum_f(hot, &sm.red);
-        const float wr_sum = block_sum_f(wr, &sm.red);
-        const int any_over = __syncthreads_or(over ? 1 : 0);
-        const long long Zsigned = static_cast<long long>(Zs);
-        if (any_over || wr_sum > 0.5f * hot_sum || Zsigned <= 0) { slow = true; reason = 2; }
+        // signed fixed point; the block sum wraps exactly
+        const unsigned long long zq = fix44(hot * f0) - fix44(wr * f0) + fix44(wp);
+        const RowSums rs = block_row_sums(sm, zq, hot, wr, over);
+        TG_T(row, 18);
+        const long long Zsigned = static_cast<long long>(rs.z);   // two's complement: the exact signed sum
+        if (rs.over || !(rs.hot < 3.0e38f) || rs.wr > 0.5f * rs.hot || Zsigned <= 0) { slow = true; reason = 2; }
+        if (nev > kEvCap) { slow = true; reason = 25; }
         const int ncand = sm.misc.ncand;
         if (!slow && ncand > kCandCap) { slow = true; reason = 4; }
         TG_DBG(row, 2, m); TG_DBG(row, 3, theta_f); TG_DBG(row, 4, static_cast<double>(Zsigned) / kFixScale);
         TG_DBG(row, 7, ncand);
         TG_T(row, 4);
         if (!slow) {
-          const FinResult fr = finalize_candidates(c, sm, m, static_cast<unsigned long long>(Zsigned), u, topk, topp);
+          const FinResult fr = finalize_candidates(c, sm, m, theta_f, static_cast<unsigned long long>(Zsigned), u, topk, topp);
           slow = !fr.ok;
           if (slow) reason = fr.reason;
           tok = fr.token;
