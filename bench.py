@@ -48,6 +48,39 @@ def dist_env():
     return rank, world, local
 
 
+CSRC = os.path.join(ROOT, "logits_processing_token_gb300", "csrc")
+PROFILE = os.path.join(ROOT, "profiles", "select_kernel_bf16_workload3.md")
+
+
+def source_digest():
+    """sha256 over the CUDA sources and the C header: names a kernel build."""
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+    for f in files + ["../../include/tg.h"]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch (read + write) from the committed ncu summary of
+    this workload, if it was taken on the current sources; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None, None
+    import re
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_traf = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_hash and m_traf):
+        return None, None
+    if m_hash.group(1) != source_digest():
+        return None, "stale (sources changed since the capture)"
+    return int(m_traf.group(1)), os.path.relpath(PROFILE, ROOT)
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -203,8 +236,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     tg.tg_clear_status(cfg)
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local, enabled=not args.no_clocks)
@@ -213,18 +244,17 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3 if clocks.proc else 0.0)
+    # back to back, as a decode loop issues them (each launch may overlap the
+    # previous one's tail through programmatic dependent launch)
     t_start.record(stream)
     for i in range(K):
-        starts[i].record(stream)
         step(i)
-        ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     flags, slow_rows = tg.tg_query_status(cfg)
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -234,7 +264,10 @@ def run_ours(args):
     value = world * B / (ms_per_step / 1000.0)
 
     alg_bytes, n_read = required_bytes(w)
-    mean_launch_s = statistics.mean(launch_ms) / 1000.0
+    # one select_kernel launch per step (B <= 512 rows per CTA): its average
+    # duration over the timed region
+    mean_launch_s = t_start.elapsed_time(t_end) / K / 1000.0
+    traffic, traffic_src = profiled_traffic()
     peak, peak_kind = measured_peak()
     achieved = alg_bytes / mean_launch_s / 1e9
     nominal_gbs = B * V * 2 / (ms_per_step / 1000.0) / 1e9
@@ -248,7 +281,7 @@ def run_ours(args):
                              (n_sets, n_sets * row_bytes / 1e6)},
             "logits_gbs": nominal_gbs, "logits_hbm_frac": nominal_gbs / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
                          "peak_source": "%s hbm_gbs (copy)" % peak_kind,
                          "bytes_per_launch": alg_bytes, "rows_reading_logits": n_read,
                          "kernel": "select_kernel<bf16>", "mean_launch_us": mean_launch_s * 1e6},
