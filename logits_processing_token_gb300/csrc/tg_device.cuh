@@ -331,22 +331,43 @@ __device__ __forceinline__ void set_bit(unsigned* bm, int t) { atomicOr(bm + (t 
 __device__ __forceinline__ bool get_bit(const unsigned* bm, int t) { return (bm[t >> 5] >> (t & 31)) & 1u; }
 
 static __device__ __noinline__ void build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
-                                  unsigned* H, unsigned* N, int nwords) {
+                                                      unsigned* H, unsigned* N, int nwords, int* stage = nullptr,
+                                                      int stage_cap = 0) {
   const int tid = threadIdx.x;
   for (int w = tid; w < nwords; w += kThreads) { H[w] = 0u; N[w] = 0u; }
-  csync();
   const int V = c.V;
   const int32_t* h = hist + r.h0;
   const int L = r.L;
+  // With a shared-memory stage large enough, the history is copied there
+  // first (coalesced, four reads in flight per thread) and every pass below
+  // reads shared memory instead of waiting on global loads one at a time.
+  const bool staged = stage != nullptr && L <= stage_cap;
+  if (staged) {
+    for (int i0 = 0; i0 < L; i0 += 4 * kThreads) {
+      int v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q * kThreads + tid;
+        v[q] = i < L ? __ldg(h + i) : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q * kThreads + tid;
+        if (i < L) stage[i] = v[q];
+      }
+    }
+  }
+  csync();
+  const int32_t* hs = staged ? stage : h;
   bool bad_id = false;
   if (c.rho != 1.0f) {
     for (int i = tid; i < L; i += kThreads) {
-      int t = __ldg(h + i);
+      int t = hs[i];
       if (t >= 0 && t < V) set_bit(H, t); else bad_id = true;
     }
   } else {
     for (int i = tid; i < L; i += kThreads) {
-      int t = __ldg(h + i);
+      int t = hs[i];
       if (t < 0 || t >= V) bad_id = true;
     }
   }
@@ -356,15 +377,15 @@ static __device__ __noinline__ void build_row_bitmaps(const DevCfg& c, const int
   if (n > 0 && L + 1 >= n) {
     const int last = L - n;  // last start of a complete n-gram
     const int s0 = L - n + 1;
-    const int first_tok = n > 1 ? __ldg(h + s0) : 0;
+    const int first_tok = n > 1 ? hs[s0] : 0;
     for (int j = tid; j <= last; j += kThreads) {
       bool eq = true;
       if (n > 1) {
-        eq = __ldg(h + j) == first_tok;
-        for (int q = 1; eq && q < n - 1; ++q) eq = __ldg(h + j + q) == __ldg(h + s0 + q);
+        eq = hs[j] == first_tok;
+        for (int q = 1; eq && q < n - 1; ++q) eq = hs[j + q] == hs[s0 + q];
       }
       if (eq) {
-        int t = __ldg(h + j + n - 1);
+        int t = hs[j + n - 1];
         if (t >= 0 && t < V) set_bit(N, t);
       }
     }

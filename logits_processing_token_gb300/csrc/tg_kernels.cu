@@ -377,9 +377,13 @@ __device__ __forceinline__ void level_find(SelSmem& sm, const T* vals, Reached r
     else { f.fb = 2 * tid + 1; f.fbefore = excl + v0; }
     f.ffound = 1;
   }
-  if (ne0 || ne1) atomicMax(&f.lastne, ne1 ? 2 * tid + 1 : 2 * tid);
   csync();
   if (!f.ffound) {
+    // nothing reached the target: the last non-empty level
+    int last = ne1 ? 2 * tid + 1 : (ne0 ? 2 * tid : -1);
+    for (int o = 16; o; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (lane == 0 && last >= 0) atomicMax(&f.lastne, last);
+    csync();
     const int L = f.lastne;
     if (L >= 0 && (L >> 1) == tid) {
       f.fb = L;
@@ -937,33 +941,42 @@ __device__ void expand_units(const DevCfg& c, SelSmem& sm, const unsigned char* 
   }
 }
 
-// End of a row: every marked token, read back and processed exactly.
-// Batches of eight per thread keep the reads in flight together.
+// End of a row: every marked token (a set bit of M), read back from global
+// memory and passed to fn(x, t).  Thread t owns bitmap words t, t+kThreads,
+// ...; it takes its tokens in batches of eight, issues a batch's eight reads
+// before using any, and every lane of a warp runs the same number of batches,
+// so the waits of a warp overlap instead of following one another.
 template <int DT, class Fn>
 __device__ __forceinline__ void for_marked(const unsigned char* rowp, const unsigned* M, int nwords, Fn fn) {
-  int tb[8];
-  int nb = 0;
-  auto flush = [&]() {
-    float xs[8];
+  constexpr int kMB = 8;
+  int cnt = 0;
+  for (int w = threadIdx.x; w < nwords; w += kThreads) cnt += __popc(M[w]);
+  int mx = cnt;
+  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int wcur = threadIdx.x;
+  unsigned bits = wcur < nwords ? M[wcur] : 0u;
+  for (int b0 = 0; b0 < mx; b0 += kMB) {
+    int tb[kMB];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) xs[q] = q < nb ? load_logit<DT>(rowp, tb[q]) : 0.0f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q < nb) fn(xs[q], tb[q]);
-    nb = 0;
-  };
-  for (int w = threadIdx.x; w < nwords; w += kThreads) {
-    unsigned bits = M[w];
-    while (bits) {
-      const int t = (w << 5) + __ffs(bits) - 1;
-      bits &= bits - 1u;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q == nb) tb[q] = t;
-      if (++nb == 8) flush();
+    for (int q = 0; q < kMB; ++q) {
+      while (bits == 0u && wcur < nwords) {
+        wcur += kThreads;
+        bits = wcur < nwords ? M[wcur] : 0u;
+      }
+      if (bits) {
+        tb[q] = (wcur << 5) + __ffs(bits) - 1;
+        bits &= bits - 1u;
+      } else {
+        tb[q] = -1;
+      }
     }
+    float xs[kMB];
+#pragma unroll
+    for (int q = 0; q < kMB; ++q) xs[q] = tb[q] >= 0 ? load_logit<DT>(rowp, tb[q]) : 0.0f;
+#pragma unroll
+    for (int q = 0; q < kMB; ++q)
+      if (tb[q] >= 0) fn(xs[q], tb[q]);
   }
-  flush();
 }
 
 // The candidates could not hold the cut or the draw: read the whole row
@@ -979,7 +992,7 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
   FinResult res{false, 20, 0u};
   csync();
   if (threadIdx.x == 0) sm.misc.ncand = 0;
-  if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords);   // ends with a barrier
+  if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
   else csync();
   expand_units<DT>(c, sm, rowp, V, 0, true, M, bitmaps, theta_raw, theta_f, tempered);
   if (bitmaps) {
@@ -1003,7 +1016,7 @@ __device__ __noinline__ unsigned slow_select(const DevCfg& c, const SelArgs& a, 
                                              float u) {
   csync();
   if (threadIdx.x == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
-  if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords);
+  if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
   RowGlobalSource<DT> src{rowp, a.V, &c, H, N, bitmaps, true};
   float mm = -INFINITY;
   src.pass([&](float s, unsigned) { mm = fmaxf(mm, s); });
@@ -1213,7 +1226,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     if (tid == 0) sm.misc.dbg_row = row;
 #endif
     TG_T(row, 0);
-    if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords);
+    // the candidate list is free at the start of a row: it stages the history
+    if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
     TG_T(row, 1);
 
     float bv = -INFINITY;            // greedy: this lane's best unmarked score and index
