@@ -156,7 +156,7 @@ struct SelSmem {
   float cand_s[kCandCap];
   unsigned cand_i[kCandCap];
   int rows[kMaxRowsPerCta];   // this CTA's streamed rows, in order
-  unsigned short ev[kEvCap];   // flagged units of the row being finished
+  unsigned ev[kEvCap];         // flagged units, then marked tokens, of the row being finished
   Hist hist;
   RedScratch red;
   Misc misc;
@@ -705,13 +705,14 @@ __device__ __forceinline__ void slice_level_counts(const Slice& sl, float m0, fl
   constexpr int NE = DT == kF32 ? 16 : 32;
   float x[NE];
   slice_values<DT>(sl, x);
-  unsigned lo4 = 0u, hi4 = 0u;   // 8-bit fields: levels 0..3 and 4..7 (at most 32 per lane)
+  // one 8-bit field per level 0..7 in a 64-bit word (at most 32 per lane); level 8 = below
+  unsigned long long f = 0ull;
 #pragma unroll
   for (int e = 0; e < NE; ++e) {
     const int l = static_cast<int>(fminf((m0 - x[e]) * inv_w, 8.0f));
-    lo4 += l < 4 ? (1u << (8 * l)) : 0u;
-    hi4 += (l >= 4 && l < 8) ? (1u << (8 * (l - 4))) : 0u;
+    f += l < 8 ? (1ull << (8 * l)) : 0ull;
   }
+  const unsigned lo4 = static_cast<unsigned>(f), hi4 = static_cast<unsigned>(f >> 32);
   unsigned v[4] = {lo4 & 0x00ff00ffu, (lo4 >> 8) & 0x00ff00ffu, hi4 & 0x00ff00ffu, (hi4 >> 8) & 0x00ff00ffu};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -813,7 +814,7 @@ __device__ __forceinline__ int list_flagged(SelSmem& sm, unsigned long long emas
     const int b = __ffsll(static_cast<long long>(emask)) - 1;
     emask &= emask - 1ull;
     if (pos < kEvCap)
-      sm.ev[pos] = static_cast<unsigned short>(((b / UPS) << 11) | (wid << 7) | (lane << 2) | (b % UPS));
+      sm.ev[pos] = static_cast<unsigned>(((b / UPS) << 11) | (wid << 7) | (lane << 2) | (b % UPS));
     ++pos;
   }
   csync();
@@ -942,35 +943,81 @@ __device__ void expand_units(const DevCfg& c, SelSmem& sm, const unsigned char* 
 }
 
 // End of a row: every marked token (a set bit of M), read back from global
-// memory and passed to fn(x, t).  Thread t owns bitmap words t, t+kThreads,
-// ...; it takes its tokens in batches of eight, issues a batch's eight reads
-// before using any, and every lane of a warp runs the same number of batches,
-// so the waits of a warp overlap instead of following one another.
+// memory and passed to fn(x, t).  The marked tokens are first listed in
+// sm.ev (block prefix over the threads' bitmap words), then thread t takes
+// list entries t, t + kThreads, ... four at a time with the four reads in
+// flight.  When more tokens are marked than the list holds, each thread walks
+// its own bitmap words instead, in batches of eight that every lane of a warp
+// runs together.  Every thread calls; sm.ev must be free.
 template <int DT, class Fn>
-__device__ __forceinline__ void for_marked(const unsigned char* rowp, const unsigned* M, int nwords, Fn fn) {
-  constexpr int kMB = 8;
+__device__ __forceinline__ void for_marked(SelSmem& sm, const unsigned char* rowp, const unsigned* M, int nwords,
+                                           Fn fn) {
+  constexpr int kMB = 4;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int cnt = 0;
   for (int w = threadIdx.x; w < nwords; w += kThreads) cnt += __popc(M[w]);
-  int mx = cnt;
-  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  int wcur = threadIdx.x;
-  unsigned bits = wcur < nwords ? M[wcur] : 0u;
-  for (int b0 = 0; b0 < mx; b0 += kMB) {
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm.misc.wu[wid] = static_cast<unsigned>(incl);
+  csync();
+  int base = 0, total = 0;
+  for (int q = 0; q < kWarps; ++q) {
+    const int cq = static_cast<int>(sm.misc.wu[q]);
+    base += q < wid ? cq : 0;
+    total += cq;
+  }
+  if (total > kEvCap) {
+    csync();
+    constexpr int kWB = 8;
+    int mx = cnt;
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int wcur = threadIdx.x;
+    unsigned bits = wcur < nwords ? M[wcur] : 0u;
+    for (int b0 = 0; b0 < mx; b0 += kWB) {
+      int tb[kWB];
+#pragma unroll
+      for (int q = 0; q < kWB; ++q) {
+        while (bits == 0u && wcur < nwords) {
+          wcur += kThreads;
+          bits = wcur < nwords ? M[wcur] : 0u;
+        }
+        if (bits) {
+          tb[q] = (wcur << 5) + __ffs(bits) - 1;
+          bits &= bits - 1u;
+        } else {
+          tb[q] = -1;
+        }
+      }
+      float xs[kWB];
+#pragma unroll
+      for (int q = 0; q < kWB; ++q) xs[q] = tb[q] >= 0 ? load_logit<DT>(rowp, tb[q]) : 0.0f;
+#pragma unroll
+      for (int q = 0; q < kWB; ++q)
+        if (tb[q] >= 0) fn(xs[q], tb[q]);
+    }
+    return;
+  }
+  int pos = base + incl - cnt;
+  for (int w = threadIdx.x; w < nwords; w += kThreads) {
+    unsigned bits = M[w];
+    while (bits) {
+      sm.ev[pos++] = static_cast<unsigned>((w << 5) + __ffs(bits) - 1);
+      bits &= bits - 1u;
+    }
+  }
+  csync();
+  for (int j0 = 0; j0 < total; j0 += kMB * kThreads) {
     int tb[kMB];
+    float xs[kMB];
 #pragma unroll
     for (int q = 0; q < kMB; ++q) {
-      while (bits == 0u && wcur < nwords) {
-        wcur += kThreads;
-        bits = wcur < nwords ? M[wcur] : 0u;
-      }
-      if (bits) {
-        tb[q] = (wcur << 5) + __ffs(bits) - 1;
-        bits &= bits - 1u;
-      } else {
-        tb[q] = -1;
-      }
+      const int j = j0 + q * kThreads + static_cast<int>(threadIdx.x);
+      tb[q] = j < total ? static_cast<int>(sm.ev[j]) : -1;
     }
-    float xs[kMB];
 #pragma unroll
     for (int q = 0; q < kMB; ++q) xs[q] = tb[q] >= 0 ? load_logit<DT>(rowp, tb[q]) : 0.0f;
 #pragma unroll
@@ -996,7 +1043,7 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
   else csync();
   expand_units<DT>(c, sm, rowp, V, 0, true, M, bitmaps, theta_raw, theta_f, tempered);
   if (bitmaps) {
-    for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
+    for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
       const float s = process_elem(c, M, N, x, t, true);
       if (s >= theta_f) {
         const int pos = atomicAdd(&sm.misc.ncand, 1);
@@ -1321,7 +1368,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     if (!SAMPLE) {
       // marked tokens, processed exactly, against the best unmarked one
       if (bitmaps) {
-        for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
+        for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
           const float s = process_elem(c, M, N, x, t, false);
           if (s > bv || (s == bv && static_cast<unsigned>(t) < bi)) { bv = s; bi = static_cast<unsigned>(t); }
         });
@@ -1375,7 +1422,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         float wr = 0.0f, wp = 0.0f;
         bool over = false;
         if (bitmaps) {
-          for_marked<DT>(rowp, M, a.nwords, [&](float x, int t) {
+          for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
             const float s = process_elem(c, M, N, x, t, true);
             wr += ex2_approx(fmaf(x, ascale, -cc0));
             wp += wfast(s, cc_m);
