@@ -145,11 +145,14 @@ struct FinSmem {
   unsigned si[kGroupCap];
   unsigned long long sw[kGroupCap];
   unsigned long long wsum[kWarps]; // per-warp partial sums of a block scan
+  unsigned wcnt[kWarps];
+  unsigned short clv[kCandCap];    // level of each candidate
   int gn;
   int fb;                          // broadcast: bucket / position
   unsigned long long fbefore;      // broadcast: mass or count before it
   int ffound;
   int lastne;                      // last non-empty level (a search that finds nothing)
+  unsigned long long fmass;        // broadcast: mass before the found level
 };
 
 struct SelSmem {
@@ -1026,6 +1029,224 @@ __device__ __forceinline__ void for_marked(SelSmem& sm, const unsigned char* row
   }
 }
 
+// Gather the candidates whose stored level is `level` into fin.g*, then sort
+// them into fin.s* by (key desc, index asc).  Returns the group size, or -1
+// when it exceeds kGroupCap.  Every thread calls.
+__device__ __noinline__ int gather_sort_stored(SelSmem& sm, int n, int level, float cc) {
+  FinSmem& f = sm.fin;
+  if (threadIdx.x == 0) f.gn = 0;
+  csync();
+  const int lane = threadIdx.x & 31;
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + threadIdx.x;
+    const bool has = i < n && f.clv[i] == level;
+    const unsigned bal = __ballot_sync(0xffffffffu, has);
+    if (bal) {
+      const int leader = __ffs(bal) - 1;
+      int pos = 0;
+      if (lane == leader) pos = atomicAdd(&f.gn, __popc(bal));
+      pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
+      if (has && pos < kGroupCap) {
+        const float s = sm.cand_s[i];
+        f.gk[pos] = fkey(s);
+        f.gi[pos] = sm.cand_i[i];
+        f.gw[pos] = wfix_fast(s, cc);
+      }
+    }
+  }
+  csync();
+  const int gn = f.gn;
+  if (gn > kGroupCap) return -1;
+  for (int t = threadIdx.x; t < gn; t += kThreads) {
+    const unsigned kt = f.gk[t], it = f.gi[t];
+    int r = 0;
+    for (int j = 0; j < gn; ++j) {
+      const unsigned kj = f.gk[j];
+      r += (kj > kt) || (kj == kt && f.gi[j] < it);
+    }
+    f.sk[r] = kt;
+    f.si[r] = it;
+    f.sw[r] = f.gw[t];
+  }
+  csync();
+  return gn;
+}
+
+// top_k, top_p and the draw over the candidate list (every candidate s is in
+// [lo, m]).  Z_all = fixed-point mass of every token of the row, relative to
+// m.  One pass sorts the candidates into kLevels value levels (count and exact
+// mass per level); one block scan gives every thread the mass and count
+// before its two levels, so each later search (the k-th token, the top-p cut,
+// the draw) is one step in which the thread owning the crossing publishes it.
+// Only the crossing level's members are sorted.  Falls back to
+// finalize_candidates when such a level holds more than kGroupCap tokens.
+__device__ __noinline__ FinResult finalize2(const DevCfg& c, SelSmem& sm, float m, float lo,
+                                           unsigned long long Z_all, float u, bool topk, bool topp) {
+  static_assert(kLevels == 2 * kThreads, "two levels per thread");
+  FinSmem& f = sm.fin;
+  FinResult res{false, 0, 0u};
+  const int n = min(sm.misc.ncand, kCandCap);
+  if (n <= 0) { res.reason = 9; return res; }
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float cc = m * kLog2e;
+  const float range = m - lo;
+  const LevelMap lv{m, range > 0.0f ? static_cast<float>(kLevels - 1) / range : 0.0f};
+  for (int l = tid; l < kLevels; l += kThreads) { f.lc[l] = 0u; f.lw[0][l] = 0u; f.lw[1][l] = 0u; f.lw[2][l] = 0u; }
+  csync();
+  for (int i = tid; i < n; i += kThreads) {
+    const float s = sm.cand_s[i];
+    const int l = lv(s);
+    f.clv[i] = static_cast<unsigned short>(l);
+    const unsigned long long w = wfix_fast(s, cc);   // <= 2^44
+    atomicAdd(&f.lc[l], 1u);
+    atomicAdd(&f.lw[0][l], static_cast<unsigned>(w & 0x7fffull));
+    atomicAdd(&f.lw[1][l], static_cast<unsigned>((w >> 15) & 0x7fffull));
+    atomicAdd(&f.lw[2][l], static_cast<unsigned>(w >> 30));
+  }
+  csync();
+  // exact mass and count of this thread's two levels, and of everything before them
+  const int l0 = 2 * tid, l1 = l0 + 1;
+  auto lmass = [&](int l) {
+    return static_cast<unsigned long long>(f.lw[0][l]) + (static_cast<unsigned long long>(f.lw[1][l]) << 15) +
+           (static_cast<unsigned long long>(f.lw[2][l]) << 30);
+  };
+  const unsigned long long m0 = lmass(l0), m1 = lmass(l1);
+  const unsigned c0 = f.lc[l0], c1 = f.lc[l1];
+  unsigned long long im = m0 + m1;
+  unsigned ic = c0 + c1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long tm = __shfl_up_sync(0xffffffffu, im, o);
+    const unsigned tc = __shfl_up_sync(0xffffffffu, ic, o);
+    if (lane >= o) { im += tm; ic += tc; }
+  }
+  if (lane == 31) { f.wsum[wid] = im; f.wcnt[wid] = ic; }
+  csync();
+  unsigned long long bm = 0ull, Zc = 0ull;
+  unsigned bc = 0u;
+  for (int q = 0; q < kWarps; ++q) {
+    const unsigned long long sq = f.wsum[q];
+    Zc += sq;
+    if (q < wid) { bm += sq; bc += f.wcnt[q]; }
+  }
+  bm += im - (m0 + m1);   // mass before level l0
+  bc += ic - (c0 + c1);   // count before level l0
+
+  unsigned long long Z;
+  int Lk = kLevels;                  // level of the k-th token (kLevels: no top_k)
+  int rk = 0;                        // kept members of level Lk (in sorted order)
+  unsigned long long kept_lk = 0ull; // their mass
+  int sorted_level = -1;             // level currently held sorted in fin.s*
+  int sorted_n = 0;
+  if (topk) {
+    const unsigned k = static_cast<unsigned>(c.top_k);
+    if (n < c.top_k) { res.reason = 4; return res; }
+    if (bc < k && bc + c0 + c1 >= k) {
+      if (bc + c0 >= k) { f.fb = l0; f.fbefore = bc; f.fmass = bm; }
+      else { f.fb = l1; f.fbefore = bc + c0; f.fmass = bm + m0; }
+    }
+    csync();
+    Lk = f.fb;
+    rk = static_cast<int>(k - static_cast<unsigned>(f.fbefore));
+    const unsigned long long before_k = f.fmass;
+    const int gn = gather_sort_stored(sm, n, Lk, cc);
+    if (gn < 0) return finalize_candidates(c, sm, m, lo, Z_all, u, topk, topp);
+    sorted_level = Lk;
+    sorted_n = gn;
+    if (tid == 0) {
+      // top_k keeps every token tied with the k-th score: extend over equal keys
+      const unsigned klo = f.sk[rk - 1];
+      int r = rk;
+      while (r < gn && f.sk[r] == klo) ++r;
+      unsigned long long s = 0ull;
+      for (int j = 0; j < r; ++j) s += f.sw[j];
+      f.fmass = s;
+      f.fb = r;
+    }
+    csync();
+    kept_lk = f.fmass;
+    rk = f.fb;
+    Z = before_k + kept_lk;
+    csync();
+  } else {
+    Z = Z_all > Zc ? Z_all : Zc;
+  }
+  // mass of level l over the kept set so far (levels past Lk dropped, Lk cut at rk)
+  auto kept_mass = [&](int l, unsigned long long ml) { return l > Lk ? 0ull : (l == Lk ? kept_lk : ml); };
+
+  unsigned long long S = Z;
+  int Lc = kLevels;                  // level of the top-p cut (kLevels: no cut)
+  int nc = 0;                        // kept members of level Lc (sorted order)
+  unsigned long long before_c = 0ull;
+  if (topp) {
+    const unsigned long long T = topp_target(c.top_p, Z);
+    if (!topk && Zc < T) { res.reason = 5; return res; }
+    if (tid == 0) f.ffound = 0;
+    csync();
+    {
+      const unsigned long long e0 = kept_mass(l0, m0), e1 = kept_mass(l1, m1);
+      if (bm < T && bm + e0 + e1 >= T) {
+        if (bm + e0 >= T) { f.fb = l0; f.fmass = bm; } else { f.fb = l1; f.fmass = bm + e0; }
+        f.ffound = 1;
+      }
+    }
+    csync();
+    if (!f.ffound) { res.reason = 6; return res; }
+    Lc = f.fb;
+    before_c = f.fmass;
+    int lim;
+    if (Lc == sorted_level) {
+      lim = Lc == Lk ? rk : sorted_n;
+    } else {
+      const int gn = gather_sort_stored(sm, n, Lc, cc);
+      if (gn < 0) return finalize_candidates(c, sm, m, lo, Z_all, u, topk, topp);
+      sorted_level = Lc;
+      sorted_n = gn;
+      lim = gn;
+    }
+    walk_sorted(sm, lim, before_c, T, false);
+    if (!f.ffound) { res.reason = 6; return res; }
+    nc = f.fb + 1;
+    S = f.fbefore + f.sw[f.fb];
+    csync();
+  }
+  const unsigned long long Td = draw_target(u, S);
+  if (!topk && !topp && !(Zc > Td)) { res.reason = 7; return res; }
+  // level of the draw among the kept levels (levels past Lc dropped, Lc cut at nc)
+  if (tid == 0) f.ffound = 0;
+  csync();
+  {
+    auto dmass = [&](int l, unsigned long long ml) {
+      if (l > Lc) return 0ull;
+      if (l == Lc) return S - before_c;
+      return kept_mass(l, ml);
+    };
+    const unsigned long long e0 = dmass(l0, m0), e1 = dmass(l1, m1);
+    if (bm <= Td && bm + e0 + e1 > Td) {
+      if (bm + e0 > Td) { f.fb = l0; f.fmass = bm; } else { f.fb = l1; f.fmass = bm + e0; }
+      f.ffound = 1;
+    }
+  }
+  csync();
+  if (!f.ffound) { res.reason = 8; return res; }
+  const int Ld = f.fb;
+  const unsigned long long before_d = f.fmass;
+  int lim;
+  if (Ld == sorted_level) {
+    lim = Ld == Lc ? nc : (Ld == Lk ? rk : sorted_n);
+  } else {
+    const int gn = gather_sort_stored(sm, n, Ld, cc);
+    if (gn < 0) return finalize_candidates(c, sm, m, lo, Z_all, u, topk, topp);
+    lim = gn;
+  }
+  walk_sorted(sm, lim, before_d, Td, true);
+  if (!f.ffound) { res.reason = 8; return res; }
+  res.token = f.si[f.fb];
+  csync();
+  res.ok = true;
+  return res;
+}
+
 // The candidates could not hold the cut or the draw: read the whole row
 // again (from L2) and take every token at or above a lower threshold.  The
 // row's total mass Z does not change.  Every thread calls.
@@ -1053,7 +1274,7 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
   }
   csync();
   if (sm.misc.ncand > kCandCap) { res.reason = 24; return res; }
-  return finalize_candidates(c, sm, m, theta_f, Z, u, topk, topp);
+  return finalize2(c, sm, m, theta_f, Z, u, topk, topp);
 }
 
 // Multi-pass exact selection over the whole row, read from global memory.
@@ -1448,7 +1669,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         TG_DBG(row, 7, ncand);
         TG_T(row, 4);
         if (!slow) {
-          const FinResult fr = finalize_candidates(c, sm, m, theta_f, static_cast<unsigned long long>(Zsigned), u, topk, topp);
+          const FinResult fr = finalize2(c, sm, m, theta_f, static_cast<unsigned long long>(Zsigned), u, topk, topp);
           slow = !fr.ok;
           if (slow) reason = fr.reason;
           tok = fr.token;
