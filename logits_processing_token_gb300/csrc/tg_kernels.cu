@@ -659,11 +659,14 @@ struct Units {
   static constexpr int kPerSlice = DT == kF32 ? 2 : 4;
 };
 
-// Sampling: the lane's raw weights 2^(x*ascale - cc0) join (ah, al); bit
+// Sampling: the lane's raw weights 2^(x*ascale - ccl) join (ah, al); bit
 // k*UPS + u of emask is set when unit u of the lane's slice in sub-chunk k
-// holds a logit at or above theta_raw.
+// holds a logit at or above theta_raw.  ccl is the lane's own reference
+// (first the block's m0 * ascale): when a slice's maximum lies more than 64
+// binary orders above it, the lane rebases its mass to that maximum, so
+// heavy-tailed rows whose maximum comes late cannot overflow.
 template <int DT>
-__device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, float cc0, float theta_raw, int k,
+__device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, float& ccl, float theta_raw, int k,
                                              float& ah, float& al, float& mxt, unsigned long long& emask) {
   constexpr int NE = DT == kF32 ? 16 : 32;
   constexpr int UPS = Units<DT>::kPerSlice;
@@ -685,8 +688,15 @@ __device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, floa
     bits |= (um[u] >= theta_raw ? 1u : 0u) << u;
   }
   mxt = fmaxf(mxt, vm);
+  const float top = vm * ascale;
+  if (top - ccl > 64.0f) {
+    const float f = ex2_approx(ccl - top);
+    ah *= f;
+    al *= f;
+    ccl = top;
+  }
   const float2 A = make_float2(ascale, ascale);
-  const float2 C = make_float2(-cc0, -cc0);
+  const float2 C = make_float2(-ccl, -ccl);
   float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
   for (int e = 0; e < NE; e += 2) {
@@ -1500,11 +1510,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
 
     float bv = -INFINITY;            // greedy: this lane's best unmarked score and index
     unsigned bi = 0xffffffffu;
-    float ah = 0.0f, al = 0.0f;      // sampling: this lane's raw mass relative to cc0 (hi + lo)
+    float ah = 0.0f, al = 0.0f;      // sampling: this lane's raw mass relative to ccl (hi + lo)
     float mxt = -INFINITY;           // sampling: largest raw logit this lane saw
     unsigned long long emask = 0ull; // sampling: units (sub-chunk, unit) of this lane that reached theta_raw
     float theta_raw = INFINITY;      // sampling: raw threshold (block-uniform)
     float ascale = kLog2e, cc0 = 0.0f;
+    float ccl = 0.0f;                // sampling: this lane's reference for its running mass
     bool decided = false;            // sampling: m0 and theta_raw are set
 
     if (tma_ok) {
@@ -1567,10 +1578,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
             theta_raw = jl >= 0 ? m0 - 2.0f * T * static_cast<float>(jl + 1) : m0;
             ascale = tempered ? kLog2e / c.temp : kLog2e;
             cc0 = m0 * ascale;
+            ccl = cc0;
             decided = true;
           }
         }
-        if (decided) slice_sample<DT>(sl, ascale, cc0, theta_raw, k, ah, al, mxt, emask);
+        if (decided) slice_sample<DT>(sl, ascale, ccl, theta_raw, k, ah, al, mxt, emask);
       }
     } else {
       // rows not on a 16-byte boundary: read the logits directly
@@ -1645,7 +1657,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         if (bitmaps) {
           for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
             const float s = process_elem(c, M, N, x, t, true);
-            wr += ex2_approx(fmaf(x, ascale, -cc0));
+            wr += ex2_approx(fmaf(x, ascale, -cc_m));
             wp += wfast(s, cc_m);
             over |= s > m;
             if (s >= theta_f) {
@@ -1654,10 +1666,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
             }
           });
         }
-        const float f0 = ex2_approx(cc0 - cc_m);   // cc0 - cc_m <= 0: m0 <= m_raw
-        const float hot = ah + al;
+        // this lane's mass relative to m (its reference ccl <= m_raw * ascale ~ cc_m)
+        const float hot = decided ? (ah + al) * ex2_approx(ccl - cc_m) : 0.0f;
         // signed fixed point; the block sum wraps exactly
-        const unsigned long long zq = fix44(hot * f0) - fix44(wr * f0) + fix44(wp);
+        const unsigned long long zq = fix44(hot) - fix44(wr) + fix44(wp);
         const RowSums rs = block_row_sums(sm, zq, hot, wr, over);
         TG_T(row, 18);
         const long long Zsigned = static_cast<long long>(rs.z);   // two's complement: the exact signed sum

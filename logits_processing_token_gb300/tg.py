@@ -207,9 +207,37 @@ def _logit_dtypes():
     return (torch.float32, torch.bfloat16, torch.int16, torch.uint16)
 
 
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_logits(t, cfg, name):
+    """The library reads rows of cfg's element type through a raw pointer:
+    the tensor's element size must match it and its last dimension must be V."""
+    want = 2 if cfg.params.get("logits_dtype", "f32") in ("bf16", 1) else 4
+    _need(t.element_size() == want, "%s has %d-byte elements; the config expects %d-byte logits"
+          % (name, t.element_size(), want))
+    _need(int(t.shape[-1]) == int(cfg.params["vocab"]), "%s has %d columns; the config's vocab is %d"
+          % (name, int(t.shape[-1]), int(cfg.params["vocab"])))
+
+
+def _check_len(t, n, name):
+    if t is not None:
+        _need(t.numel() >= n, "%s holds %d elements; the call needs %d" % (name, t.numel(), n))
+
+
 def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms, out_ids, stream=None):
+    """logits [B, V]; hist_offsets [B+1]; prompt_lens [B]; uniforms [B] (sampling); out_ids [B].
+    The history ids that hist_offsets point at are not bounds-checked here: they live on the device."""
     import torch
+    _need(logits.dim() == 2, "logits must be [B, V]")
+    _check_logits(logits, cfg, "logits")
     B, V = int(logits.shape[0]), int(logits.shape[-1])
+    _check_len(hist_offsets, B + 1, "hist_offsets")
+    _check_len(prompt_lens, B, "prompt_lens")
+    _check_len(uniforms, B, "uniforms")
+    _check_len(out_ids, B, "out_ids")
     st = load_library().tg_select(
         _ptr(logits, "logits", _logit_dtypes()), B, V,
         _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
@@ -221,8 +249,17 @@ def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms
 
 
 def tg_verify(target_logits, cand_ids, K: int, cfg: Config, uniforms, out_match, out_next, stream=None):
+    """target_logits [B, K+1, V]; cand_ids [B, K]; uniforms [B, K+1] (sampling);
+    out_match [B]; out_next [B, K+1]."""
     import torch
+    _need(target_logits.dim() == 3 and int(target_logits.shape[1]) == int(K) + 1,
+          "target_logits must be [B, K+1, V]")
+    _check_logits(target_logits, cfg, "target_logits")
     B, V = int(target_logits.shape[0]), int(target_logits.shape[-1])
+    _check_len(cand_ids, B * int(K), "cand_ids")
+    _check_len(uniforms, B * (int(K) + 1), "uniforms")
+    _check_len(out_match, B, "out_match")
+    _check_len(out_next, B * (int(K) + 1), "out_next")
     st = load_library().tg_verify(
         _ptr(target_logits, "target_logits", _logit_dtypes()), B, V, _ptr(cand_ids, "cand_ids", (torch.int32,)),
         int(K), cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
@@ -234,7 +271,14 @@ def tg_verify(target_logits, cand_ids, K: int, cfg: Config, uniforms, out_match,
 def tg_process(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, out_scores, out_banbits=None,
                out_probs=None, stream=None):
     import torch
+    _need(logits.dim() == 2, "logits must be [B, V]")
+    _check_logits(logits, cfg, "logits")
     B, V = int(logits.shape[0]), int(logits.shape[-1])
+    _check_len(hist_offsets, B + 1, "hist_offsets")
+    _check_len(prompt_lens, B, "prompt_lens")
+    _check_len(out_scores, B * V, "out_scores")
+    _check_len(out_banbits, B * ((V + 31) // 32), "out_banbits")
+    _check_len(out_probs, B * V, "out_probs")
     st = load_library().tg_process(
         _ptr(logits, "logits", _logit_dtypes()), B, V,
         _ptr(hist_ids, "hist_ids", (torch.int32,)) if hist_ids is not None and hist_ids.numel() else None,

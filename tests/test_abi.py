@@ -96,3 +96,40 @@ def test_null_arguments_rejected(lib):
     assert lib.tg_select(None, 1, 10, None, None, None, None, None, None, None) == tg.TG_ERR_INVALID_ARGUMENT
     assert lib.tg_verify(None, 1, 10, None, 1, None, None, None, None, None) == tg.TG_ERR_INVALID_ARGUMENT
     assert lib.tg_config_destroy(None) == tg.TG_ERR_INVALID_ARGUMENT
+
+
+def test_binding_rejects_mis_shaped_tensors():
+    """The C ABI takes raw pointers and cannot see buffer extents, so the
+    binding checks shapes and element sizes before any call."""
+    import types
+    import torch
+    import logits_processing_token_gb300 as tg
+    cfg32 = types.SimpleNamespace(params=dict(vocab=64, logits_dtype="f32"), handle=None)
+    cfg16 = types.SimpleNamespace(params=dict(vocab=64, logits_dtype="bf16"), handle=None)
+    i32 = torch.int32
+    # verify targets must be [B, K+1, V]: a flattened [B*(K+1), V] would make B too large
+    with pytest.raises(ValueError, match=r"\[B, K\+1, V\]"):
+        tg.tg_verify(torch.zeros(3 * 5, 64), torch.zeros(3, 4, dtype=i32), 4, cfg32, None,
+                     torch.zeros(3, dtype=i32), torch.zeros(3, 5, dtype=i32))
+    with pytest.raises(ValueError, match="out_next"):
+        tg.tg_verify(torch.zeros(3, 5, 64), torch.zeros(3, 4, dtype=i32), 4, cfg32, None,
+                     torch.zeros(3, dtype=i32), torch.zeros(3, 4, dtype=i32))
+    with pytest.raises(ValueError, match="cand_ids"):
+        tg.tg_verify(torch.zeros(3, 5, 64), torch.zeros(3, 3, dtype=i32), 4, cfg32, None,
+                     torch.zeros(3, dtype=i32), torch.zeros(3, 5, dtype=i32))
+    # element size and vocabulary must match the config
+    with pytest.raises(ValueError, match="2-byte"):
+        tg.tg_select(torch.zeros(2, 64), None, torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=i32),
+                     cfg16, None, torch.zeros(2, dtype=i32))
+    with pytest.raises(ValueError, match="vocab"):
+        tg.tg_select(torch.zeros(2, 63), None, torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=i32),
+                     cfg32, None, torch.zeros(2, dtype=i32))
+    with pytest.raises(ValueError, match="hist_offsets"):
+        tg.tg_select(torch.zeros(2, 64), None, torch.zeros(2, dtype=torch.int64), torch.zeros(2, dtype=i32),
+                     cfg32, None, torch.zeros(2, dtype=i32))
+    with pytest.raises(ValueError, match="out_ids"):
+        tg.tg_select(torch.zeros(2, 64), None, torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=i32),
+                     cfg32, None, torch.zeros(1, dtype=i32))
+    with pytest.raises(ValueError, match="out_scores"):
+        tg.tg_process(torch.zeros(2, 64), None, torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=i32),
+                      cfg32, torch.zeros(2, 63))
