@@ -579,6 +579,7 @@ __device__ __forceinline__ FindOut<T> warp_find(const T* v, const unsigned* cnt,
 struct Hist {
   unsigned long long mass[256];
   unsigned cnt[256];
+  unsigned mw[4][256];   // the weights in four 11-bit limbs: exact sums with 32-bit atomics
   // broadcast slots
   unsigned sel_bucket;
   unsigned long long sel_above;
@@ -609,7 +610,11 @@ struct MassSel {
 
 // Clear the histogram (all threads) -- followed by a barrier.
 __device__ __forceinline__ void hist_clear(Hist* h) {
-  for (int i = threadIdx.x; i < 256; i += kThreads) { h->mass[i] = 0ull; h->cnt[i] = 0u; }
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    h->mass[i] = 0ull;
+    h->cnt[i] = 0u;
+    h->mw[0][i] = 0u; h->mw[1][i] = 0u; h->mw[2][i] = 0u; h->mw[3][i] = 0u;
+  }
   csync();
 }
 
@@ -683,10 +688,18 @@ __device__ MassSel mass_select(const Src& src, Flt flt, Wt wf, unsigned long lon
       unsigned key = fkey(s);
       if (flt(key, i) && (key & hi_mask) == prefix) {
         unsigned b = (key >> shift) & 255u;
-        atomicAdd(&h->mass[b], wf(s));
+        const unsigned long long w = wf(s);   // <= 2^44
+        atomicAdd(&h->mw[0][b], static_cast<unsigned>(w & 0x7ffull));
+        atomicAdd(&h->mw[1][b], static_cast<unsigned>((w >> 11) & 0x7ffull));
+        atomicAdd(&h->mw[2][b], static_cast<unsigned>((w >> 22) & 0x7ffull));
+        atomicAdd(&h->mw[3][b], static_cast<unsigned>(w >> 33));
         atomicAdd(&h->cnt[b], 1u);
       }
     });
+    csync();
+    for (int i = threadIdx.x; i < 256; i += kThreads)
+      h->mass[i] = static_cast<unsigned long long>(h->mw[0][i]) + (static_cast<unsigned long long>(h->mw[1][i]) << 11) +
+                   (static_cast<unsigned long long>(h->mw[2][i]) << 22) + (static_cast<unsigned long long>(h->mw[3][i]) << 33);
     csync();
     if (threadIdx.x < 32) {
       const unsigned long long base = above;

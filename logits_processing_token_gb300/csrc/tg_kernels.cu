@@ -202,15 +202,45 @@ struct RowGlobalSource {
   const unsigned* N;
   bool bitmaps;
   bool sample;
+  __device__ __forceinline__ float score(float x, int i) const {
+    if (bitmaps) return process_elem(*c, H, N, x, i, sample);
+    if (sample && c->temp != 1.0f) return clampf(__fdiv_rn(x, c->temp));
+    return x;
+  }
+  // Every token of the row once.  A 16-byte aligned row is read a vector
+  // (16 bytes) per thread at a time, two vectors in flight; the tail and an
+  // unaligned row element by element.
   template <class Fn>
   __device__ __forceinline__ void pass(Fn f) const {
-    for (int i = threadIdx.x; i < V; i += kThreads) {
-      const float x = load_logit<DT>(row, i);
-      float s = x;
-      if (bitmaps) s = process_elem(*c, H, N, x, i, sample);
-      else if (sample && c->temp != 1.0f) s = clampf(__fdiv_rn(x, c->temp));
-      f(s, static_cast<unsigned>(i));
+    constexpr int PER = DT == kF32 ? 4 : 8;
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) {
+      const int nvec = V / PER;
+      const uint4* rv = static_cast<const uint4*>(row);
+      for (int v0 = 0; v0 < nvec; v0 += 2 * kThreads) {
+        uint4 q[2];
+        int vi[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          vi[h] = v0 + h * kThreads + static_cast<int>(threadIdx.x);
+          q[h] = vi[h] < nvec ? __ldg(rv + vi[h]) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (vi[h] < nvec) {
+            const unsigned ps[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+#pragma unroll
+            for (int e = 0; e < PER; ++e) {
+              const float x = DT == kF32 ? __uint_as_float(ps[e]) : ((e & 1) ? bf16hi(ps[e >> 1]) : bf16lo(ps[e >> 1]));
+              const int i = vi[h] * PER + e;
+              f(score(x, i), static_cast<unsigned>(i));
+            }
+          }
+        }
+      }
+      done = nvec * PER;
     }
+    for (int i = done + static_cast<int>(threadIdx.x); i < V; i += kThreads) f(score(load_logit<DT>(row, i), i), static_cast<unsigned>(i));
   }
 };
 
@@ -659,19 +689,26 @@ struct Units {
   static constexpr int kPerSlice = DT == kF32 ? 2 : 4;
 };
 
-// Sampling: the lane's raw weights 2^(x*ascale - ccl) join (ah, al); bit
+// Sampling: the lane's raw weights 2^(x*ascale - ccl) over its unmarked tokens join (ah, al); bit
 // k*UPS + u of emask is set when unit u of the lane's slice in sub-chunk k
 // holds a logit at or above theta_raw.  ccl is the lane's own reference
 // (first the block's m0 * ascale): when a slice's maximum lies more than 64
 // binary orders above it, the lane rebases its mass to that maximum, so
 // heavy-tailed rows whose maximum comes late cannot overflow.
 template <int DT>
-__device__ __forceinline__ void slice_sample(const Slice& sl, float ascale, float& ccl, float theta_raw, int k,
-                                             float& ah, float& al, float& mxt, unsigned long long& emask) {
+__device__ __forceinline__ void slice_sample(const Slice& sl, int tok0, const unsigned* M, bool bitmaps, float ascale,
+                                             float& ccl, float theta_raw, int k, float& ah, float& al, float& mxt,
+                                             unsigned long long& emask) {
   constexpr int NE = DT == kF32 ? 16 : 32;
   constexpr int UPS = Units<DT>::kPerSlice;
   float x[NE];
   slice_values<DT>(sl, x);
+  if (bitmaps) {
+    // marked tokens are merged exactly at the end of the row: they count nothing here
+    const unsigned mk = slice_marks<DT>(sl, tok0, M);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) x[e] = ((mk >> e) & 1u) ? -INFINITY : x[e];
+  }
   float um[UPS];
 #pragma unroll
   for (int u = 0; u < UPS; ++u) {
@@ -1553,6 +1590,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
           {
             float x[4 * PER];
             slice_values<DT>(sl, x);
+            if (bitmaps) {
+              const unsigned mk = slice_marks<DT>(sl, tok0, M);
+#pragma unroll
+              for (int e = 0; e < 4 * PER; ++e) x[e] = ((mk >> e) & 1u) ? -INFINITY : x[e];
+            }
             mx = tree_max<4 * PER>(x);
           }
           const float m0 = block_max(mx, &sm.red);
@@ -1582,7 +1624,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
             decided = true;
           }
         }
-        if (decided) slice_sample<DT>(sl, ascale, ccl, theta_raw, k, ah, al, mxt, emask);
+        if (decided) slice_sample<DT>(sl, tok0, M, bitmaps, ascale, ccl, theta_raw, k, ah, al, mxt, emask);
       }
     } else {
       // rows not on a 16-byte boundary: read the logits directly
@@ -1643,37 +1685,39 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       const float T = tempered ? c.temp : 1.0f;
       // every unmarked token with a processed score >= theta_f has x >= theta_raw
       const float theta_f = tempered ? nextafterf(__fdiv_rn(theta_raw, T), INFINITY) : theta_raw;
-      const float m = tempered ? clampf(__fdiv_rn(m_raw, T)) : m_raw;   // >= every unmarked score
-      const float cc_m = m * kLog2e;
+      float m = tempered ? clampf(__fdiv_rn(m_raw, T)) : m_raw;   // >= every unmarked score
+      float cc_m = m * kLog2e;
       if (!slow) {
         const int nev = list_flagged<DT>(sm, emask);
         TG_T(row, 16);
         expand_units<DT>(c, sm, rowp, V, nev, false, M, bitmaps, theta_raw, theta_f, tempered);
         TG_T(row, 17);
         TG_T(row, 3);
-        // the hot mass counted marked tokens at their raw weight: swap in the processed one
-        float wr = 0.0f, wp = 0.0f;
-        bool over = false;
+        // marked tokens, processed exactly: their weight (against a thread-local
+        // reference, raised when a processed score exceeds it) and their maximum
+        float wp = 0.0f, pref = cc_m, mk_max = -INFINITY;
         if (bitmaps) {
           for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
             const float s = process_elem(c, M, N, x, t, true);
-            wr += ex2_approx(fmaf(x, ascale, -cc_m));
-            wp += wfast(s, cc_m);
-            over |= s > m;
+            const float sc = s * kLog2e;
+            if (sc > pref) { wp *= ex2_approx(pref - sc); pref = sc; }
+            wp += ex2_approx(sc - pref);
+            mk_max = fmaxf(mk_max, s);
             if (s >= theta_f) {
               const int pos = atomicAdd(&sm.misc.ncand, 1);
               if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = static_cast<unsigned>(t); }
             }
           });
         }
-        // this lane's mass relative to m (its reference ccl <= m_raw * ascale ~ cc_m)
+        // the reference maximum of the row: the larger of the unmarked maximum and the marked scores
+        m = fmaxf(m, block_max(mk_max, &sm.red));
+        cc_m = m * kLog2e;
         const float hot = decided ? (ah + al) * ex2_approx(ccl - cc_m) : 0.0f;
-        // signed fixed point; the block sum wraps exactly
-        const unsigned long long zq = fix44(hot) - fix44(wr) + fix44(wp);
-        const RowSums rs = block_row_sums(sm, zq, hot, wr, over);
+        const float zl = hot + wp * ex2_approx(pref - cc_m);
+        const RowSums rs = block_row_sums(sm, fix44(zl), hot, 0.0f, false);
         TG_T(row, 18);
-        const long long Zsigned = static_cast<long long>(rs.z);   // two's complement: the exact signed sum
-        if (rs.over || !(rs.hot < 3.0e38f) || rs.wr > 0.5f * rs.hot || Zsigned <= 0) { slow = true; reason = 2; }
+        const long long Zsigned = static_cast<long long>(rs.z);
+        if (!(rs.hot < 3.0e38f) || Zsigned <= 0) { slow = true; reason = 2; }
         if (nev > kEvCap) { slow = true; reason = 25; }
         const int ncand = sm.misc.ncand;
         if (!slow && ncand > kCandCap) { slow = true; reason = 4; }
