@@ -100,6 +100,7 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned 
 }
 // Bounded wait: false after ~1 s without completion.
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (static_cast<unsigned long long>(clock64() - t0) > kWaitLimitCycles) return false;
@@ -1505,13 +1506,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     __syncthreads();
   }
   const int nrow = sm.misc.nrow;
-  const long long total_seq = static_cast<long long>(nrow) * nsub;
+  const int total_seq = nrow * nsub;   // <= kMaxRowsPerCta * (TG_MAX_VOCAB * 4 / kStageBytes)
 
-  // Load sub-chunk `q` of the schedule (row q / nsub, sub-chunk q % nsub) into its stage.
-  auto issue = [&](long long q) {
-    const int st = static_cast<int>(q % nst);
-    const int row = sm.rows[q / nsub];
-    const int kk = static_cast<int>(q % nsub);
+  // Load sub-chunk kk of the schedule's row ri into stage st.
+  auto issue = [&](int st, int ri, int kk) {
+    const int row = sm.rows[ri];
     const int lo = kk * SE, n = min(SE, V - lo);
     const unsigned char* src = static_cast<const unsigned char*>(a.logits) + (static_cast<size_t>(row) * V + lo) * esz;
     mbar_expect_tx(&sm.misc.full[st], static_cast<unsigned>(n * esz));
@@ -1519,10 +1518,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     sm.misc.iss[st] += 1;
   };
   if (tma_ok && tid == 0) {
-    for (long long q = 0; q < nst && q < total_seq; ++q) issue(q);
+    for (int q = 0; q < nst && q < total_seq; ++q) issue(q, q / nsub, q % nsub);
   }
   grid_dependents_launch();
 
+  int cur_st = 0;          // stage and phase of the next sub-chunk of the schedule
+  unsigned cur_ph = 0u;
   for (int ri = 0; ri < nrow; ++ri) {
     const int row = sm.rows[ri];
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
@@ -1557,9 +1558,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
 
     if (tma_ok) {
       for (int k = 0; k < nsub; ++k) {
-        const long long seq = static_cast<long long>(ri) * nsub + k;
-        const int st = static_cast<int>(seq % nst);
-        const unsigned parity = static_cast<unsigned>((seq / nst) & 1);
+        const int st = cur_st;
+        const unsigned parity = cur_ph;
+        if (++cur_st == nst) { cur_st = 0; cur_ph ^= 1u; }
         if (!*reinterpret_cast<volatile int*>(&sm.misc.error)) {
           if (!mbar_wait(&sm.misc.full[st], parity)) atomicExch(&sm.misc.error, 1);
         }
@@ -1577,7 +1578,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
           if ((done & (kWarps - 1)) == kWarps - 1) {
             __threadfence_block();
             fence_proxy_async();
-            if (seq + nst < total_seq && !*reinterpret_cast<volatile int*>(&sm.misc.error)) issue(seq + nst);
+            // the stage's next use: sub-chunk k + nst of this row, or of a later one
+            int nk = k + nst, nri = ri;
+            while (nk >= nsub) { nk -= nsub; ++nri; }
+            if (nri < nrow && !*reinterpret_cast<volatile int*>(&sm.misc.error)) issue(st, nri, nk);
           }
         }
         if (!SAMPLE) {
