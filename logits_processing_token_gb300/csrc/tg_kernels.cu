@@ -78,6 +78,12 @@ __device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// Shared-memory atomic add with acquire-release ordering at block scope.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -1573,10 +1579,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         // the slice is in registers; the sixteenth warp to get here refills the stage
         __syncwarp();
         if (lane == 0) {
-          __threadfence_block();
-          const unsigned done = atomicAdd(&sm.misc.cnt[st], 1u);
+          // release: this warp's reads of the stage happen before the count;
+          // acquire (for the sixteenth): every warp's reads happen before the refill
+          const unsigned done = atom_add_acq_rel(&sm.misc.cnt[st], 1u);
           if ((done & (kWarps - 1)) == kWarps - 1) {
-            __threadfence_block();
             fence_proxy_async();
             // the stage's next use: sub-chunk k + nst of this row, or of a later one
             int nk = k + nst, nri = ri;
