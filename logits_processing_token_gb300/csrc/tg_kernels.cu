@@ -215,27 +215,31 @@ struct RowGlobalSource {
     return x;
   }
   // Every token of the row once.  A 16-byte aligned row is read a vector
-  // (16 bytes) per thread at a time, two vectors in flight; the tail and an
+  // (16 bytes) per thread at a time, four vectors in flight; the tail and an
   // unaligned row element by element.
   template <class Fn>
   __device__ __forceinline__ void pass(Fn f) const {
     constexpr int PER = DT == kF32 ? 4 : 8;
+    constexpr int NV = 4;
     int done = 0;
     if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) {
       const int nvec = V / PER;
       const uint4* rv = static_cast<const uint4*>(row);
-      for (int v0 = 0; v0 < nvec; v0 += 2 * kThreads) {
-        uint4 q[2];
-        int vi[2];
+      for (int v0 = 0; v0 < nvec; v0 += NV * kThreads) {
+        uint4 q[NV];
+        int vi[NV];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NV; ++h) {
           vi[h] = v0 + h * kThreads + static_cast<int>(threadIdx.x);
           q[h] = vi[h] < nvec ? __ldg(rv + vi[h]) : make_uint4(0u, 0u, 0u, 0u);
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+        for (int h = 0; h < NV; ++h) {
           if (vi[h] < nvec) {
-            const unsigned ps[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+            uint4 v = q[0];
+#pragma unroll
+            for (int hh = 1; hh < NV; ++hh) v = hh == h ? q[hh] : v;
+            const unsigned ps[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < PER; ++e) {
               const float x = DT == kF32 ? __uint_as_float(ps[e]) : ((e & 1) ? bf16hi(ps[e >> 1]) : bf16lo(ps[e >> 1]));
@@ -1331,7 +1335,213 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
   return finalize2(c, sm, m, theta_f, Z, u, topk, topp);
 }
 
-// Multi-pass exact selection over the whole row, read from global memory.
+struct LevelPick {
+  bool ok;
+  unsigned idx;                 // the selected token
+  unsigned long long cum;       // mass of every token up to and including it
+};
+
+// The first candidate, in (score desc, index asc) order over the list
+// cand_s/cand_i[0..n) (every score in [lo, hi]), at which the running mass
+// (weights relative to cc / log2e) reaches `target` (>= target, or > target
+// when strict).  `base` is added to the returned running mass.  A level
+// histogram over [lo, hi] finds the level; only its members are sorted.
+// Every thread calls.  Uses FinSmem (which aliases the row bitmaps).
+__device__ __forceinline__ LevelPick list_pick(SelSmem& sm, int n, float hi, float lo, float cc,
+                                            unsigned long long target, bool strict, unsigned long long base) {
+  FinSmem& f = sm.fin;
+  LevelPick res{false, 0u, 0ull};
+  if (n <= 0) return res;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float range = hi - lo;
+  const LevelMap lv{hi, range > 0.0f ? static_cast<float>(kLevels - 1) / range : 0.0f};
+  for (int l = tid; l < kLevels; l += kThreads) { f.lc[l] = 0u; f.lw[0][l] = 0u; f.lw[1][l] = 0u; f.lw[2][l] = 0u; }
+  csync();
+  for (int i = tid; i < n; i += kThreads) {
+    const float s = sm.cand_s[i];
+    const int l = lv(s);
+    f.clv[i] = static_cast<unsigned short>(l);
+    const unsigned long long w = wfix_fast(s, cc);
+    atomicAdd(&f.lc[l], 1u);
+    atomicAdd(&f.lw[0][l], static_cast<unsigned>(w & 0x7fffull));
+    atomicAdd(&f.lw[1][l], static_cast<unsigned>((w >> 15) & 0x7fffull));
+    atomicAdd(&f.lw[2][l], static_cast<unsigned>(w >> 30));
+  }
+  csync();
+  const int l0 = 2 * tid, l1 = l0 + 1;
+  auto lmass = [&](int l) {
+    return static_cast<unsigned long long>(f.lw[0][l]) + (static_cast<unsigned long long>(f.lw[1][l]) << 15) +
+           (static_cast<unsigned long long>(f.lw[2][l]) << 30);
+  };
+  const unsigned long long m0 = lmass(l0), m1 = lmass(l1);
+  unsigned long long im = m0 + m1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long tm = __shfl_up_sync(0xffffffffu, im, o);
+    if (lane >= o) im += tm;
+  }
+  if (lane == 31) f.wsum[wid] = im;
+  if (tid == 0) f.ffound = 0;
+  csync();
+  unsigned long long bm = 0ull;
+  for (int q = 0; q < wid; ++q) bm += f.wsum[q];
+  bm += im - (m0 + m1);
+  auto reached = [&](unsigned long long x) { return strict ? x > target : x >= target; };
+  if (!reached(bm) && reached(bm + m0 + m1)) {
+    if (reached(bm + m0)) { f.fb = l0; f.fmass = bm; } else { f.fb = l1; f.fmass = bm + m0; }
+    f.ffound = 1;
+  }
+  csync();
+  if (!f.ffound) return res;
+  const int L = f.fb;
+  const unsigned long long before = f.fmass;
+  const int gn = gather_sort_stored(sm, n, L, cc);
+  if (gn < 0) return res;
+  walk_sorted(sm, gn, before, target, strict);
+  if (!f.ffound) return res;
+  res.ok = true;
+  res.idx = f.si[f.fb];
+  res.cum = base + f.fbefore + f.sw[f.fb];
+  csync();
+  return res;
+}
+
+// Items whose key (order-preserving score key) lies in [klo, khi).
+struct InWindow {
+  unsigned klo, khi;
+  __device__ __forceinline__ bool operator()(unsigned key, unsigned) const { return key >= klo && key < khi; }
+};
+struct AtLeast {
+  unsigned k;
+  __device__ __forceinline__ bool operator()(unsigned key, unsigned) const { return key >= k; }
+};
+
+
+// The first token, in (score desc, index asc) order over the whole row, at
+// which the running mass (exact weights relative to m) reaches `target`
+// (>= target, or > target when strict).  m >= every score; only tokens with
+// score > m - 32 can carry mass at the 2^-44 quantum.  One pass counts the
+// tokens in 2,048 levels of 1/64 below m; the level where the estimated
+// running mass (count x the level's middle weight, rescaled to the exact
+// total Z) crosses the target gives a narrow score window; one pass sums the
+// exact mass above the window and inside it; when the target lies inside,
+// the radix selection runs over the window's few tokens.  ok = false when
+// four windows miss.  Every thread calls; the candidate list is free.
+template <int DT>
+__device__ __forceinline__ LevelPick level_pick(const RowGlobalSource<DT>& src, SelSmem& sm, float m,
+                                             unsigned long long Z, unsigned long long target, bool strict) {
+  constexpr int kL = 2048;
+  constexpr float kPer = 64.0f;   // levels per score unit
+  static_assert(kEvCap >= 2048, "level counts live in the unit list");
+  unsigned* cnt = sm.ev;
+  LevelPick res{false, 0u, 0ull};
+  for (int l = threadIdx.x; l < kL; l += kThreads) cnt[l] = 0u;
+  csync();
+  src.pass([&](float s, unsigned) {
+    const float d = (m - s) * kPer;
+    if (d < static_cast<float>(kL)) atomicAdd(&cnt[d > 0.0f ? static_cast<int>(d) : 0], 1u);
+  });
+  csync();
+  // estimated mass of each level (relative to m); thread t owns levels 4t .. 4t+3
+  {
+    constexpr int PT = kL / kThreads;
+    static_assert(kL % kThreads == 0, "levels per thread");
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    float e[PT];
+    float loc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < PT; ++j) {
+      const int l = PT * static_cast<int>(threadIdx.x) + j;
+      e[j] = static_cast<float>(cnt[l]) * expf(-(static_cast<float>(l) + 0.5f) / kPer);
+      loc += e[j];
+    }
+    float incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) sm.misc.wf[wid] = incl;
+    if (threadIdx.x == 0) sm.misc.wu[0] = static_cast<unsigned>(kL - 1);
+    csync();
+    float before = 0.0f, tot = 0.0f;
+    for (int q = 0; q < kWarps; ++q) {
+      const float v = sm.misc.wf[q];
+      tot += v;
+      before += q < wid ? v : 0.0f;
+    }
+    before += incl - loc;
+    // the exact total rescales the estimate; the target in the same units
+    const float unit = 1.0f / 17592186044416.0f;
+    const float scale = tot > 0.0f ? (static_cast<float>(Z) * unit) / tot : 1.0f;
+    const float want = static_cast<float>(target) * unit / scale;
+    if (before < want && before + loc >= want) {
+      float run = before;
+      int le_t = PT * static_cast<int>(threadIdx.x) + PT - 1;
+#pragma unroll
+      for (int j = 0; j < PT; ++j) {
+        run += e[j];
+        if (run >= want) { le_t = PT * static_cast<int>(threadIdx.x) + j; break; }
+      }
+      sm.misc.wu[0] = static_cast<unsigned>(le_t);
+    }
+    csync();
+  }
+  int le = static_cast<int>(sm.misc.wu[0]);
+  const WFast wx{m * kLog2e};
+  for (int attempt = 0, half = 3; attempt < 4; ++attempt, half *= 4) {
+    // window (m - l1/64, m - l0/64], narrowed until its tokens fit the list
+    int l0 = 0, l1 = 0;
+    unsigned wn = 0u;
+    for (int h = half;; h >>= 1) {
+      l0 = max(0, le - h);
+      l1 = min(kL, le + h + 1);
+      unsigned t = 0u;
+      for (int l = l0 + static_cast<int>(threadIdx.x); l < l1; l += kThreads) t += cnt[l];
+      wn = static_cast<unsigned>(block_sum_u64(t, &sm.red));
+      if (wn <= static_cast<unsigned>(kCandCap) || h == 0) break;
+    }
+    if (wn > static_cast<unsigned>(kCandCap)) break;
+    // keys: higher score = larger key
+    const unsigned khi = l0 == 0 ? 0xffffffffu : fkey(m - static_cast<float>(l0) / kPer);
+    const unsigned klo = l1 >= kL ? 0u : fkey(m - static_cast<float>(l1) / kPer);
+    // exact mass above the window, and the window's tokens gathered into the
+    // candidate list, in one pass
+    if (threadIdx.x == 0) sm.misc.ncand = 0;
+    csync();
+    unsigned long long a_t = 0ull, w_t = 0ull;
+    src.pass([&](float s, unsigned i) {
+      const unsigned key = fkey(s);
+      bool in = false;
+      if (key >= klo) {
+        const unsigned long long w = wx(s);
+        if (key >= khi) a_t += w; else { w_t += w; in = true; }
+      }
+      if (in) {
+        const int pos = atomicAdd(&sm.misc.ncand, 1);
+        if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = i; }
+      }
+    });
+    const unsigned long long A = block_sum_u64(a_t, &sm.red);
+    const unsigned long long W = block_sum_u64(w_t, &sm.red);
+    const bool below = strict ? target < A : target <= A;            // the crossing is above the window
+    const bool past = strict ? target >= A + W : target > A + W;     // ... or below it
+    if (!below && !past) {
+      const int nw = min(sm.misc.ncand, kCandCap);
+      const float top = l0 == 0 ? m : m - static_cast<float>(l0) / kPer;
+      const float bot = m - static_cast<float>(l1) / kPer;
+      return list_pick(sm, nw, top, bot, m * kLog2e, target - A, strict, A);
+    }
+    if (below && l0 == 0) break;
+    if (past && l1 >= kL) break;
+    le = below ? max(0, l0 - 1) : min(kL - 1, l1);
+  }
+  return res;
+}
+
+// Multi-pass exact selection over the whole row, read from global memory
+// (it is normally in L2).  top_k rows run the generic radix selection;
+// the others locate the top-p cut and the draw with level_pick.
 template <int DT>
 __device__ __noinline__ unsigned slow_select(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
                                              const unsigned char* rowp, unsigned* H, unsigned* N, bool bitmaps,
@@ -1343,6 +1553,31 @@ __device__ __noinline__ unsigned slow_select(const DevCfg& c, const SelArgs& a, 
   float mm = -INFINITY;
   src.pass([&](float s, unsigned) { mm = fmaxf(mm, s); });
   mm = block_max(mm, &sm.red);
+  const bool topk = c.top_k > 0 && static_cast<unsigned>(c.top_k) < static_cast<unsigned>(a.V);
+  if (!topk && mm > kFilter) {
+    unsigned long long z_t = 0ull;
+    const WFast wz{mm * kLog2e};
+    src.pass([&](float s, unsigned) { z_t += wz(s); });
+    const unsigned long long Z = block_sum_u64(z_t, &sm.red);
+    unsigned long long S = Z;
+    bool ok = Z > 0ull;
+    // an exact pick over a window uses the finishing area, which holds the
+    // row bitmaps: they are rebuilt before the next pass that reads them
+    auto restore = [&]() {
+      if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+    };
+    if (ok && c.top_p < 1.0f) {
+      const LevelPick cut = level_pick<DT>(src, sm, mm, Z, topp_target(c.top_p, Z), false);
+      restore();
+      ok = cut.ok;
+      S = cut.cum;
+    }
+    if (ok) {
+      const LevelPick d = level_pick<DT>(src, sm, mm, Z, draw_target(u, S), true);
+      if (d.ok) return d.idx;
+    }
+    restore();
+  }
   return sample_exact(c, src, mm, u, static_cast<unsigned>(a.V), &sm.hist, &sm.red, nullptr, nullptr);
 }
 
@@ -1741,7 +1976,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
           tok = fr.token;
           // Too little candidate mass for the cut or draw: one more pass, read
           // directly (the row is likely still in L2), with a lower threshold.
-          if (slow && (reason == 5 || reason == 7)) {
+          // (a draw without top_p that misses its target lies in the bulk of the
+          // row; only the exact path helps there)
+          if (slow && reason == 5) {
             TG_T(row, 5);
             const FinResult fr2 = second_chance<DT>(c, a, sm, rm, rowp, M, N, bitmaps, theta_raw - 2.0f * T, tempered, m,
                                                     static_cast<unsigned long long>(Zsigned), u, topk, topp);
