@@ -54,32 +54,27 @@ std::vector<int> sorted_unique(std::initializer_list<std::pair<const int32_t*, i
   return v;
 }
 
-// Pick the TMA ring depth: two CTAs per SM when the ring can still hold three
-// stages, else one CTA per SM with a deeper ring.
+// Pick the TMA ring depth.  One CTA per SM (512 threads at 128 registers
+// fill the register file); three stages of 32 KB keep a row's stream fed, and
+// a deeper ring measured slower (less L1 for the row-end reads, more of the
+// next row prefetched while the row end runs); two when three do not fit.
 tg_status plan_select(int dtype, bool verify, int nwords, LaunchPlan* out) {
-  int dev = 0, per_sm = 0, optin = 0, reserved = 0;
+  int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
   if (e != cudaSuccess) return from_cuda(e);
   const int base = tg::select_smem_bytes(0, nwords);
-  for (int ctas = 2; ctas >= 1; --ctas) {
-    int budget = std::min(optin, per_sm / ctas - reserved);
-    int ns = std::min(8, (budget - base) / tg::kStageBytes);
-    if (ns < (ctas == 2 ? 3 : 2)) continue;
-    int smem = tg::select_smem_bytes(ns, nwords);
-    int occ = 0;
-    e = tg::select_occupancy(dtype, verify, smem, &occ);
-    if (e != cudaSuccess) return from_cuda(e);
-    if (occ >= ctas || (ctas == 1 && occ >= 1)) {
-      out->nstage = ns;
-      out->smem = smem;
-      out->blocks_per_sm = ctas;
-      return TG_OK;
-    }
-  }
-  return TG_ERR_UNSUPPORTED;
+  const int ns = std::min(tg::kRingStages, (optin - base) / tg::kStageBytes);
+  if (ns < 2) return TG_ERR_UNSUPPORTED;
+  const int smem = tg::select_smem_bytes(ns, nwords);
+  int occ = 0;
+  e = tg::select_occupancy(dtype, verify, smem, &occ);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (occ < 1) return TG_ERR_UNSUPPORTED;
+  out->nstage = ns;
+  out->smem = smem;
+  out->blocks_per_sm = 1;
+  return TG_OK;
 }
 
 tg_status check_device(const tg_config* cfg) {

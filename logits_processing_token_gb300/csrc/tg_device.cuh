@@ -15,6 +15,7 @@ namespace tg {
 constexpr int kThreads = 512;               // threads per CTA of every kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kStageBytes = 32768;          // one TMA bulk copy / sub-chunk of a row
+constexpr int kRingStages = 3;              // TMA ring depth when it fits (else two)
 constexpr int kCandCap = 4096;              // candidate slots of the one-pass path
 constexpr float kFilter = -3.40282346638528859812e+38f;  // -FLT_MAX
 constexpr float kLog2e = 1.44269504088896340736f;

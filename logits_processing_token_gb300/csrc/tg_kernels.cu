@@ -871,12 +871,17 @@ __device__ __forceinline__ int list_flagged(SelSmem& sm, unsigned long long emas
     total += cq;
   }
   int pos = base + incl - cnt;
-  while (emask) {
-    const int b = __ffsll(static_cast<long long>(emask)) - 1;
-    emask &= emask - 1ull;
-    if (pos < kEvCap)
-      sm.ev[pos] = static_cast<unsigned>(((b / UPS) << 11) | (wid << 7) | (lane << 2) | (b % UPS));
-    ++pos;
+  const unsigned tag = static_cast<unsigned>((wid << 7) | (lane << 2));
+  // the two halves in turn: 32-bit bit scans are half the work of 64-bit ones
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    unsigned bits = static_cast<unsigned>(half ? (emask >> 32) : emask);
+    while (bits) {
+      const unsigned b = static_cast<unsigned>(__ffs(bits) - 1) + 32u * half;
+      bits &= bits - 1u;
+      if (pos < kEvCap) sm.ev[pos] = ((b / UPS) << 11) | tag | (b % UPS);
+      ++pos;
+    }
   }
   csync();
   return total;
@@ -2168,7 +2173,7 @@ cudaError_t noalloc_setup(int dev, NoAllocDevice** out) {
     int optin = 0;
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     for (int dt = 0; dt < 2 && e == cudaSuccess; ++dt) {
-      const int ns = min(8, (optin - select_smem_bytes(0, 0)) / kStageBytes);
+      const int ns = min(kRingStages, (optin - select_smem_bytes(0, 0)) / kStageBytes);
       d.nstage[dt] = ns;
       d.smem[dt] = select_smem_bytes(ns, 0);
       e = select_occupancy(dt, true, d.smem[dt], &d.bps[dt]);
