@@ -331,9 +331,16 @@ __device__ __forceinline__ RowMeta row_meta(const DevCfg& c, const int32_t* hist
 __device__ __forceinline__ void set_bit(unsigned* bm, int t) { atomicOr(bm + (t >> 5), 1u << (t & 31)); }
 __device__ __forceinline__ bool get_bit(const unsigned* bm, int t) { return (bm[t >> 5] >> (t & 31)) & 1u; }
 
-static __device__ __noinline__ void build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
-                                                      unsigned* H, unsigned* N, int nwords, int* stage = nullptr,
-                                                      int stage_cap = 0) {
+//
+// With `ctr` (a shared counter) and the history staged, the marked tokens are
+// also listed, each once, in N's words (entry = t | banned << 31) and the
+// count is returned; N then no longer holds the banned bitmap.  The return
+// value is -1 when no list is made (not asked for, history not staged, or
+// more marked tokens than fit), and N keeps the bitmap.
+constexpr unsigned kBannedFlag = 0x80000000u;
+static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
+                                                     unsigned* H, unsigned* N, int nwords, int* stage = nullptr,
+                                                     int stage_cap = 0, unsigned* ctr = nullptr) {
   const int tid = threadIdx.x;
   for (int w = tid; w < nwords; w += kThreads) { H[w] = 0u; N[w] = 0u; }
   const int V = c.V;
@@ -396,10 +403,65 @@ static __device__ __noinline__ void build_row_bitmaps(const DevCfg& c, const int
   if (r.bsup)
     for (int i = tid; i < c.n_bsup; i += kThreads) set_bit(N, __ldg(c.bsup_sorted + i));
   if (bad_id) atomicOr(c.status, kFlagBadId);
+  const bool listing = ctr != nullptr && staged;
+  if (listing && tid == 0) *ctr = 0u;
   csync();
   // H becomes the marked set M = history | banned; N stays the banned set
-  for (int w = tid; w < nwords; w += kThreads) H[w] |= N[w];
+  int cnt = 0;
+  for (int w = tid; w < nwords; w += kThreads) {
+    const unsigned m = H[w] | N[w];
+    H[w] = m;
+    cnt += __popc(m);
+  }
+  if (!listing) {
+    csync();
+    return -1;
+  }
+  // The list: every marked token is a history id or an id of a ban list.
+  // The first thread to clear a token's bit in M lists it; M is restored
+  // from the list afterwards.  A warp reserves room for its entries at once.
+  for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((tid & 31) == 0) atomicAdd(ctr, static_cast<unsigned>(cnt));
   csync();
+  const int total = static_cast<int>(*ctr);
+  const int cap = min(stage_cap - L, nwords);
+  csync();
+  if (total > cap) return -1;
+  if (tid == 0) *ctr = 0u;
+  csync();
+  int* tmp = stage + L;
+  const int lane = tid & 31;
+  auto claim = [&](int t) {   // every lane of the warp calls, t < 0 for none
+    bool own = false;
+    unsigned e = 0u;
+    if (t >= 0 && t < V) {
+      const unsigned bit = 1u << (t & 31);
+      own = (atomicAnd(&H[t >> 5], ~bit) & bit) != 0u;
+      e = static_cast<unsigned>(t) | ((N[t >> 5] & bit) ? kBannedFlag : 0u);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, own);
+    if (bal) {
+      int base = 0;
+      if (lane == 0) base = static_cast<int>(atomicAdd(ctr, static_cast<unsigned>(__popc(bal))));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (own) tmp[base + __popc(bal & ((1u << lane) - 1u))] = static_cast<int>(e);
+    }
+  };
+  for (int i0 = 0; i0 < L; i0 += kThreads) claim(i0 + tid < L ? hs[i0 + tid] : -1);
+  for (int i0 = 0; i0 < c.n_ban; i0 += kThreads) claim(i0 + tid < c.n_ban ? __ldg(c.ban_sorted + i0 + tid) : -1);
+  if (r.eos_off) claim(tid < c.n_eos ? c.eos[tid] : -1);
+  if (r.bsup)
+    for (int i0 = 0; i0 < c.n_bsup; i0 += kThreads) claim(i0 + tid < c.n_bsup ? __ldg(c.bsup_sorted + i0 + tid) : -1);
+  csync();
+  const int nl = static_cast<int>(*ctr);
+  const bool whole = nl == total;   // always, unless a marked token had no source
+  for (int i = tid; i < nl; i += kThreads) {
+    const unsigned e = static_cast<unsigned>(tmp[i]);
+    if (whole) N[i] = e;
+    atomicOr(&H[(e & ~kBannedFlag) >> 5], 1u << (e & 31u));
+  }
+  csync();
+  return whole ? nl : -1;
 }
 
 // Processed score of one token from its raw value and the row bitmaps
@@ -409,6 +471,15 @@ __device__ __forceinline__ float process_elem(const DevCfg& c, const unsigned* H
   float s = x;
   if (get_bit(N, i)) s = kFilter;
   else if (get_bit(H, i)) s = penalize(x, c.rho);
+  if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
+  return s;
+}
+
+// Processed score of a marked token (its row-bitmap bit is set) from its raw
+// value: the filter value when banned, else penalised; then temperature when
+// sampling.  The same result as process_elem for such a token.
+__device__ __forceinline__ float process_marked(const DevCfg& c, float x, bool banned, bool sample) {
+  float s = banned ? kFilter : penalize(x, c.rho);
   if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
   return s;
 }

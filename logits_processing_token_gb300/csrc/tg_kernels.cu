@@ -129,6 +129,7 @@ struct Misc {
   int iss[kMaxStages];                   // copies issued into each stage
   int nrow;                              // streamed rows of this CTA
   int ncand;                             // candidates in the list
+  unsigned lctr;                         // counter of the marked-token list while it is built
   int error;                             // a wait timed out; the kernel stops loading
   int err_snap;                          // thread 0's snapshot of `error`, read by all threads
   int gcause;                            // debug builds: why a row left the one-pass path
@@ -389,6 +390,30 @@ __device__ __forceinline__ void walk_sorted(SelSmem& sm, int cnt, unsigned long 
     }
   }
   csync();
+}
+
+// End of a row, listed marked tokens: entry j of list[0..n) (t | banned
+// << 31) is read back from global memory and passed to fn(x, t, banned, j).
+// Thread t takes entries t, t + kThreads, ... four at a time with the four
+// reads in flight.
+template <int DT, class Fn>
+__device__ __forceinline__ void for_listed(const unsigned* list, int n, const unsigned char* rowp, Fn fn) {
+  constexpr int kMB = 4;
+  for (int j0 = 0; j0 < n; j0 += kMB * kThreads) {
+    unsigned e[kMB];
+    float xs[kMB];
+#pragma unroll
+    for (int q = 0; q < kMB; ++q) {
+      const int j = j0 + q * kThreads + static_cast<int>(threadIdx.x);
+      e[q] = j < n ? list[j] : 0xffffffffu;
+    }
+#pragma unroll
+    for (int q = 0; q < kMB; ++q) xs[q] = e[q] != 0xffffffffu ? load_logit<DT>(rowp, static_cast<int>(e[q] & ~kBannedFlag)) : 0.0f;
+#pragma unroll
+    for (int q = 0; q < kMB; ++q)
+      if (e[q] != 0xffffffffu)
+        fn(xs[q], static_cast<int>(e[q] & ~kBannedFlag), (e[q] & kBannedFlag) != 0u, j0 + q * kThreads + static_cast<int>(threadIdx.x));
+  }
 }
 
 // Block-wide search over the levels: the first level l where the running
@@ -1789,7 +1814,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
 #endif
     TG_T(row, 0);
     // the candidate list is free at the start of a row: it stages the history
-    if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+    // the marked tokens are listed too (in N's words) when they fit
+    const int nlist = bitmaps ? build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s),
+                                                  2 * kCandCap, &sm.misc.lctr)
+                              : -1;
     TG_T(row, 1);
 
     float bv = -INFINITY;            // greedy: this lane's best unmarked score and index
@@ -1892,11 +1920,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     int token = -1;
     if (!SAMPLE) {
       // marked tokens, processed exactly, against the best unmarked one
-      if (bitmaps) {
-        for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
-          const float s = process_elem(c, M, N, x, t, false);
-          if (s > bv || (s == bv && static_cast<unsigned>(t) < bi)) { bv = s; bi = static_cast<unsigned>(t); }
-        });
+      auto merge = [&](float s, int t) {
+        if (s > bv || (s == bv && static_cast<unsigned>(t) < bi)) { bv = s; bi = static_cast<unsigned>(t); }
+      };
+      if (bitmaps && nlist >= 0) {
+        for_listed<DT>(N, nlist, rowp, [&](float x, int t, bool banned, int) { merge(process_marked(c, x, banned, false), t); });
+      } else if (bitmaps) {
+        for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) { merge(process_elem(c, M, N, x, t, false), t); });
       }
       for (int o = 16; o; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -1946,25 +1976,44 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         // marked tokens, processed exactly: their weight (against a thread-local
         // reference, raised when a processed score exceeds it) and their maximum
         float wp = 0.0f, pref = cc_m, mk_max = -INFINITY;
-        if (bitmaps) {
+        auto push = [&](float s, int t) {
+          if (s >= theta_f) {
+            const int pos = atomicAdd(&sm.misc.ncand, 1);
+            if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = static_cast<unsigned>(t); }
+          }
+        };
+        if (bitmaps && nlist >= 0) {
+          // listed: each processed score replaces its entry; the weights follow once m is known
+          for_listed<DT>(N, nlist, rowp, [&](float x, int t, bool banned, int j) {
+            const float s = process_marked(c, x, banned, true);
+            mk_max = fmaxf(mk_max, s);
+            push(s, t);
+            N[j] = __float_as_uint(s);
+          });
+        } else if (bitmaps) {
+          // their weight against a thread-local reference, raised when a processed score exceeds it
           for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) {
             const float s = process_elem(c, M, N, x, t, true);
             const float sc = s * kLog2e;
             if (sc > pref) { wp *= ex2_approx(pref - sc); pref = sc; }
             wp += ex2_approx(sc - pref);
             mk_max = fmaxf(mk_max, s);
-            if (s >= theta_f) {
-              const int pos = atomicAdd(&sm.misc.ncand, 1);
-              if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = static_cast<unsigned>(t); }
-            }
+            push(s, t);
           });
         }
         // the reference maximum of the row: the larger of the unmarked maximum and the marked scores
         m = fmaxf(m, block_max(mk_max, &sm.red));
         cc_m = m * kLog2e;
         const float hot = decided ? (ah + al) * ex2_approx(ccl - cc_m) : 0.0f;
-        const float zl = hot + wp * ex2_approx(pref - cc_m);
-        const RowSums rs = block_row_sums(sm, fix44(zl), hot, 0.0f, false);
+        unsigned long long zt;
+        if (bitmaps && nlist >= 0) {
+          // exact per-token weights: the same integers the candidates carry
+          zt = fix44(hot);
+          for (int j = tid; j < nlist; j += kThreads) zt += wfix_fast(__uint_as_float(N[j]), cc_m);
+        } else {
+          zt = fix44(hot + wp * ex2_approx(pref - cc_m));
+        }
+        const RowSums rs = block_row_sums(sm, zt, hot, 0.0f, false);
         TG_T(row, 18);
         const long long Zsigned = static_cast<long long>(rs.z);
         if (!(rs.hot < 3.0e38f) || Zsigned <= 0) { slow = true; reason = 2; }
