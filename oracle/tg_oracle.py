@@ -96,6 +96,7 @@ class RowInfo:
     u_boundary: bool = False         # u within BOUNDARY_EPS of a CDF value
     n_kept: int = 0                  # tokens kept for the draw
     forced: bool = False
+    logprob: float = float("nan")    # log-softmax of the selected-from scores at the token
 
 
 # ---------------------------------------------------------------------------
@@ -326,19 +327,44 @@ def final_distribution(s_t: np.ndarray, p: Params) -> np.ndarray:
     return out
 
 
+def log_softmax_at(scores: np.ndarray, tok: int) -> float:
+    """Transmuter.Generation, section "Log-probabilities": the log-softmax of
+    the scores a step selects from, at the selected token, in fp64:
+    s_tok - m - log(sum_i exp(s_i - m)) with m the largest score.  Removed
+    tokens hold the filter value and add exp(F - m) = 0, unless every token
+    is removed (then all are equal and the result is -log V)."""
+    d = scores.astype(np.float64)
+    m = d.max()
+    return float(d[tok] - m - np.log(np.sum(np.exp(d - m))))
+
+
+def selected_from_scores(s_t: np.ndarray, order: np.ndarray, n_kept: int, s_k: np.ndarray) -> np.ndarray:
+    """The scores a sampling step selects from: after the processors and
+    temperature, top_k (``s_k``, removed tokens at the filter value) and top_p
+    (tokens past the kept prefix of the order at the filter value)."""
+    out = np.full(s_t.size, FILTER, dtype=F32)
+    kept = order[:n_kept]
+    out[kept] = s_k[kept]
+    return out
+
+
 def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float):
-    """One row of tg_select.  Returns (token id or -1, RowInfo)."""
+    """One row of tg_select.  Returns (token id or -1, RowInfo); the info
+    carries the token's log-probability (NaN for a padding row)."""
     if len(h) == 0:
         return -1, RowInfo()
     s, _, info = process_row(x, h, P, p)
     if p.mode == "greedy":
-        return int(np.argmax(s)), info
+        tok = int(np.argmax(s))
+        info.logprob = log_softmax_at(s, tok)
+        return tok, info
     s_t = apply_temperature(s, p)
-    order, n_kept, probs, _, dinfo = sample_distribution(s_t, p)
+    order, n_kept, probs, s_k, dinfo = sample_distribution(s_t, p)
     tok, ub = draw(order, n_kept, probs, u)
     info.topp_boundary = dinfo.topp_boundary
     info.u_boundary = ub
     info.n_kept = n_kept
+    info.logprob = log_softmax_at(selected_from_scores(s_t, order, n_kept, s_k), tok)
     return tok, info
 
 

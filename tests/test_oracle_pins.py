@@ -385,3 +385,90 @@ def test_identity_settings_leave_scores_unchanged():
         p.top_k = k
         _, n_kept, probs, filt, _ = O.sample_distribution(st, p)
         assert n_kept == 64 and np.array_equal(filt, x)
+
+
+# --------------------------------------------------------------------------
+# token log-probabilities (Transmuter.Generation, section "Log-probabilities":
+# the log-softmax of the scores the step selects from, at the token)
+# --------------------------------------------------------------------------
+def test_logprob_two_tokens_closed_form():
+    a, b = 2.5, 0.75
+    x = np.array([a, b], np.float32)
+    g = O.select_row(x, [0], 1, P(vocab=2), 0.0)[1].logprob
+    assert g == pytest.approx(-math.log1p(math.exp(float(x[1]) - float(x[0]))), abs=1e-13)
+    # sampling: a high uniform draws the second token; temperature divides first
+    T = 0.5
+    tok, info = O.select_row(x, [0], 1, P(vocab=2, mode="sample", temperature=T), 0.999)
+    sa, sb = float(np.float32(x[0] / np.float32(T))), float(np.float32(x[1] / np.float32(T)))
+    assert tok == 1
+    assert info.logprob == pytest.approx((sb - sa) - math.log1p(math.exp(sb - sa)), abs=1e-12)
+
+
+def test_logprob_over_the_kept_set():
+    """Each kept token, drawn in turn, has log-probability s_i - log(sum over
+    the kept set of exp(s_j)); the kept set is rebuilt here by sorting and
+    math.fsum, independently of the oracle; the probabilities sum to one."""
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        V = int(rng.integers(4, 14))
+        x = rng.normal(0, 2, V).astype(np.float32)
+        T = float(rng.choice([1.0, 0.7]))
+        k = int(rng.integers(0, V + 1))
+        pp = float(rng.choice([1.0, 0.8, 0.5]))
+        params = P(vocab=V, mode="sample", temperature=T, top_k=k, top_p=pp)
+        s = (x / np.float32(T)).astype(np.float32) if T != 1.0 else x.copy()
+        order = sorted(range(V), key=lambda i: (-float(s[i]), i))
+        if 0 < k < V:
+            tau = float(s[order[k - 1]])
+            order = [i for i in order if float(s[i]) >= tau]
+        m = float(s[order[0]])
+        w = [math.exp(float(s[i]) - m) for i in order]
+        tot = math.fsum(w)
+        kept = len(order)
+        if pp < 1.0:
+            cum = 0.0
+            for j in range(len(order)):
+                cum = math.fsum(w[: j + 1]) / tot
+                if cum >= pp:
+                    kept = j + 1
+                    break
+            if abs(cum - pp) < 1e-9 or (kept >= 2 and abs(math.fsum(w[: kept - 1]) / tot - pp) < 1e-9):
+                continue
+        ks = math.fsum(w[:kept])
+        probs = []
+        for j in range(kept):
+            lo, hi = math.fsum(w[:j]) / ks, math.fsum(w[: j + 1]) / ks
+            if hi - lo < 1e-6:
+                continue
+            tok, info = O.select_row(x, [0], 1, params, (lo + hi) / 2)
+            assert tok == order[j]
+            expect = (float(s[tok]) - m) - math.log(ks)
+            assert info.logprob == pytest.approx(expect, abs=1e-12)
+            probs.append(math.exp(info.logprob))
+        if len(probs) == kept:
+            assert math.fsum(probs) == pytest.approx(1.0, abs=1e-12)
+
+
+def test_logprob_equal_scores():
+    V = 7
+    x = np.full(V, 1.25, np.float32)
+    assert O.select_row(x, [0], 1, P(vocab=V), 0.0)[1].logprob == pytest.approx(-math.log(V), abs=1e-14)
+    # top_k keeps every token tied at the k-th score
+    info = O.select_row(x, [0], 1, P(vocab=V, mode="sample", top_k=3), 0.4)[1]
+    assert info.logprob == pytest.approx(-math.log(V), abs=1e-14)
+    # top_p over equal scores keeps the shortest prefix with mass >= p: ceil(p V) tokens
+    info = O.select_row(x, [0], 1, P(vocab=V, mode="sample", top_p=0.5), 0.4)[1]
+    assert info.logprob == pytest.approx(-math.log(4), abs=1e-14)
+    # every token removed: the scores are all the filter value, each -log V
+    info = O.select_row(x, [0], 1, P(vocab=V, suppress_tokens=list(range(V))), 0.0)[1]
+    assert info.logprob == pytest.approx(-math.log(V), abs=1e-14)
+
+
+def test_logprob_forced_and_padding_rows():
+    V = 10
+    x = np.linspace(-1, 1, V).astype(np.float32)
+    # forced eos with two eos ids at L = P + max_new - 1: both score 0, the rest the filter value
+    p = P(vocab=V, eos_token_ids=[3, 7], forced_eos_token_ids=[3, 7], max_new_tokens=4)
+    tok, info = O.select_row(x, [1, 2, 5, 6], 1, p, 0.0)
+    assert tok == 3 and info.logprob == pytest.approx(-math.log(2), abs=1e-14)
+    assert math.isnan(O.select_row(x, [], 0, p, 0.0)[1].logprob)
