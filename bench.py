@@ -38,6 +38,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--logprobs", action="store_true",
+                    help="time tg_select_logprobs (ids plus each token's log-probability) instead of tg_select")
     return ap.parse_args()
 
 
@@ -226,10 +228,11 @@ def run_ours(args):
     pl = torch.from_numpy(w.prompt_lens).cuda()
     u = torch.from_numpy(w.uniforms).cuda()
     out = torch.empty(B, dtype=torch.int32, device="cuda")
+    lp = torch.empty(B, dtype=torch.float32, device="cuda") if args.logprobs else None
     stream = torch.cuda.current_stream()
 
     def step(i):
-        tg.tg_select(sets[i % n_sets], hid, off, pl, cfg, u, out, stream=stream)
+        tg.tg_select(sets[i % n_sets], hid, off, pl, cfg, u, out, stream=stream, out_logprobs=lp)
 
     for i in range(args.warmup):
         step(i)
@@ -278,7 +281,8 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "B": B, "V": V, "logits_dtype": "bf16", "rows_per_gpu": B,
                        "parallelism": "replicas (rows independent, no collective)",
                        "l2": "inputs rotate over %d copies of the logits (%.0f MB) > L2" %
-                             (n_sets, n_sets * row_bytes / 1e6)},
+                             (n_sets, n_sets * row_bytes / 1e6),
+                       "logprobs": bool(args.logprobs)},
             "logits_gbs": nominal_gbs, "logits_hbm_frac": nominal_gbs / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
@@ -297,9 +301,10 @@ def run_ours(args):
         h_pl = torch.from_numpy(w.prompt_lens).pin_memory()
         h_u = torch.from_numpy(w.uniforms).pin_memory()
         h_out = torch.empty(B, dtype=torch.int32).pin_memory()
+        h_lp = torch.empty(B, dtype=torch.float32).pin_memory() if lp is not None else None
         d_logits = torch.empty_like(h_logits, device="cuda")
         bi = sum(t.numel() * t.element_size() for t in (h_logits, h_hid, h_off, h_pl, h_u))
-        bo = h_out.numel() * 4
+        bo = h_out.numel() * 4 + (h_lp.numel() * 4 if h_lp is not None else 0)
 
         def e2e_step():
             d_logits.copy_(h_logits, non_blocking=True)
@@ -307,8 +312,10 @@ def run_ours(args):
             off.copy_(h_off, non_blocking=True)
             pl.copy_(h_pl, non_blocking=True)
             u.copy_(h_u, non_blocking=True)
-            tg.tg_select(d_logits.view(torch.bfloat16), hid, off, pl, cfg, u, out, stream=stream)
+            tg.tg_select(d_logits.view(torch.bfloat16), hid, off, pl, cfg, u, out, stream=stream, out_logprobs=lp)
             h_out.copy_(out, non_blocking=True)
+            if lp is not None:
+                h_lp.copy_(lp, non_blocking=True)
 
         for _ in range(3):
             e2e_step()

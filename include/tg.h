@@ -146,6 +146,28 @@ tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* his
                     tg_stream stream);
 
 /*
+ * tg_select_logprobs -- tg_select, plus the log-probability of each row's
+ * token (Transmuter.Generation, section "Log-probabilities"): the
+ * log-softmax, at the token, of the scores the step selects from.  For
+ * greedy rows those are the processed scores; for sampled rows the
+ * processed scores after temperature, with every token outside the kept
+ * top_k / top_p set removed.
+ *
+ *  out_logprobs  device f32 [B]; NaN for an empty row.  Computed from the
+ *                token's score and the kept set's 44-bit fixed-point mass
+ *                (about 1e-7 relative); out_ids as tg_select gives them.
+ *
+ * Other arguments, layouts and errors as tg_select; out_logprobs must not be
+ * NULL.  A greedy config runs the sampling kernel with temperature, top_k
+ * and top_p off and u = 0 (the first token of the (score desc, index asc)
+ * order is the argmax with the lowest index), so the row's mass is summed.
+ */
+tg_status tg_select_logprobs(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                             const int64_t* hist_offsets, const int32_t* prompt_lens,
+                             const tg_config* cfg, const float* uniforms, int32_t* out_ids,
+                             float* out_logprobs, tg_stream stream);
+
+/*
  * tg_verify -- assisted-generation verification (Assisted Generation,
  * "Greedy decoding with assisted generation", steps 3-5).
  *

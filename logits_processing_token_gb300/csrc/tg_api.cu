@@ -205,16 +205,28 @@ tg_status tg_config_destroy(tg_config* cfg) {
   return from_cuda(e != cudaSuccess ? e : e2);
 }
 
-tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
-                    const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
-                    const float* uniforms, int32_t* out_ids, tg_stream stream) {
+namespace {
+tg_status select_impl(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                      const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                      const float* uniforms, int32_t* out_ids, float* out_logprobs, tg_stream stream) {
   if (!cfg || B < 0 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
   if (B == 0) return TG_OK;
   if (!logits || !hist_offsets || !prompt_lens || !out_ids) return TG_ERR_INVALID_ARGUMENT;
   if (cfg->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
   tg_status st = check_device(cfg);
   if (st != TG_OK) return st;
+  // Log-probabilities come from the sampling kernel, which sums the row's
+  // mass: a greedy config runs it with the warpers off and u = 0.
+  tg::DevCfg dev = cfg->dev;
+  if (out_logprobs && cfg->mode == TG_GREEDY) {
+    dev.mode = tg::kSample;
+    dev.temp = 1.0f;
+    dev.top_k = 0;
+    dev.top_p = 1.0f;
+    uniforms = nullptr;
+  }
   tg::SelArgs a{};
+  a.logprobs = out_logprobs;
   a.logits = logits;
   a.nrows = B;
   a.nrows_total = B;
@@ -227,7 +239,22 @@ tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* his
   a.nstage = cfg->sel.nstage;
   a.nwords = cfg->nwords;
   int grid = std::min<long long>(B, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm);
-  return from_cuda(tg::launch_select(cfg->dev, a, false, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(tg::launch_select(dev, a, false, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                    const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                    const float* uniforms, int32_t* out_ids, tg_stream stream) {
+  return select_impl(logits, B, V, hist_ids, hist_offsets, prompt_lens, cfg, uniforms, out_ids, nullptr, stream);
+}
+
+tg_status tg_select_logprobs(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                             const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                             const float* uniforms, int32_t* out_ids, float* out_logprobs, tg_stream stream) {
+  if (!out_logprobs && B > 0) return TG_ERR_INVALID_ARGUMENT;
+  return select_impl(logits, B, V, hist_ids, hist_offsets, prompt_lens, cfg, uniforms, out_ids, out_logprobs,
+                     stream);
 }
 
 tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids, int32_t K,

@@ -75,6 +75,7 @@ struct SelArgs {
   const int32_t* cand;   // verify
   int K;
   int32_t* out_match;
+  float* logprobs;       // select: the token's log-probability per row, or null
   int nstage;
   int nwords;
 };
@@ -832,7 +833,7 @@ __device__ unsigned count_items(const Src& src, Flt flt, RedScratch* red) {
 template <class Src>
 __device__ unsigned sample_exact(const DevCfg& c, const Src& src, float m, float u, unsigned V,
                                  Hist* h, RedScratch* red, KeepFilter* kept_out,
-                                 unsigned long long* S_out) {
+                                 unsigned long long* S_out, unsigned* key_out = nullptr) {
   KeepFilter f{0u, false, 0u, 0u};
   if (c.top_k > 0 && static_cast<unsigned>(c.top_k) < V)
     f.klo = kth_key(src, f, static_cast<unsigned>(c.top_k), h);
@@ -851,6 +852,7 @@ __device__ unsigned sample_exact(const DevCfg& c, const Src& src, float m, float
   MassSel d = mass_select(src, f, wx, Td, true, h);
   if (kept_out) *kept_out = f;
   if (S_out) *S_out = S;
+  if (key_out) *key_out = d.key;
   return d.idx;
 }
 

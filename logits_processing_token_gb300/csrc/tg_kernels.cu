@@ -474,9 +474,11 @@ __device__ __forceinline__ void level_limit(SelSmem& sm, int L, unsigned long lo
 }
 
 struct FinResult {
-  bool ok;        // false: the candidates cannot decide this row
+  bool ok;                 // false: the candidates cannot decide this row
   int reason;
   unsigned token;
+  float score;             // the token's processed score
+  unsigned long long S;    // mass of the kept set (weights relative to the row maximum)
 };
 
 // top_k, top_p and the draw over the candidates.  Z_all = fixed-point mass
@@ -592,19 +594,23 @@ __device__ __noinline__ FinResult finalize_candidates(const DevCfg& c, SelSmem& 
   if (Ld == Lc && cut_sorted) {
     walk_sorted(sm, nc, before, Td, true);
     res.token = f.si[f.fb];
+    res.score = key2f(f.sk[f.fb]);
   } else {
     const int gn = gather_sort_level(sm, n, lv, Ld, klo, cc);
     if (gn >= 0) {
       const int lim = (Ld == Lc) ? nc : gn;
       walk_sorted(sm, lim, before, Td, true);
       res.token = f.si[f.fb];
+      res.score = key2f(f.sk[f.fb]);
     } else {
       CandLevelSource ls{sm.cand_s, sm.cand_i, n, lv, Ld};
       MassSel d = mass_select(ls, keep, wf, Td - before, true, &sm.hist);
       if (!d.found) { res.reason = 8; return res; }
       res.token = d.idx;
+      res.score = key2f(d.key);
     }
   }
+  res.S = S;
   csync();
   TG_TF(14);
   res.ok = true;
@@ -1330,6 +1336,8 @@ __device__ __noinline__ FinResult finalize2(const DevCfg& c, SelSmem& sm, float 
   walk_sorted(sm, lim, before_d, Td, true);
   if (!f.ffound) { res.reason = 8; return res; }
   res.token = f.si[f.fb];
+  res.score = key2f(f.sk[f.fb]);
+  res.S = S;
   csync();
   res.ok = true;
   return res;
@@ -1368,6 +1376,7 @@ __device__ __noinline__ FinResult second_chance(const DevCfg& c, const SelArgs& 
 struct LevelPick {
   bool ok;
   unsigned idx;                 // the selected token
+  unsigned key;                 // its order-preserving score key
   unsigned long long cum;       // mass of every token up to and including it
 };
 
@@ -1380,7 +1389,7 @@ struct LevelPick {
 __device__ __forceinline__ LevelPick list_pick(SelSmem& sm, int n, float hi, float lo, float cc,
                                             unsigned long long target, bool strict, unsigned long long base) {
   FinSmem& f = sm.fin;
-  LevelPick res{false, 0u, 0ull};
+  LevelPick res{false, 0u, 0u, 0ull};
   if (n <= 0) return res;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const float range = hi - lo;
@@ -1431,6 +1440,7 @@ __device__ __forceinline__ LevelPick list_pick(SelSmem& sm, int n, float hi, flo
   if (!f.ffound) return res;
   res.ok = true;
   res.idx = f.si[f.fb];
+  res.key = f.sk[f.fb];
   res.cum = base + f.fbefore + f.sw[f.fb];
   csync();
   return res;
@@ -1464,7 +1474,7 @@ __device__ __forceinline__ LevelPick level_pick(const RowGlobalSource<DT>& src, 
   constexpr float kPer = 64.0f;   // levels per score unit
   static_assert(kEvCap >= 2048, "level counts live in the unit list");
   unsigned* cnt = sm.ev;
-  LevelPick res{false, 0u, 0ull};
+  LevelPick res{false, 0u, 0u, 0ull};
   for (int l = threadIdx.x; l < kL; l += kThreads) cnt[l] = 0u;
   csync();
   src.pass([&](float s, unsigned) {
@@ -1572,8 +1582,15 @@ __device__ __forceinline__ LevelPick level_pick(const RowGlobalSource<DT>& src, 
 // Multi-pass exact selection over the whole row, read from global memory
 // (it is normally in L2).  top_k rows run the generic radix selection;
 // the others locate the top-p cut and the draw with level_pick.
+struct SlowPick {
+  unsigned token;
+  float score;            // its processed score
+  float ref;              // the masses' reference: m * log2e (fast weights) or m (accurate weights)
+  bool fast;              // weights 2^(s * log2e - ref) (ex2.approx), else exp(s - ref)
+  unsigned long long S;   // mass of the kept set
+};
 template <int DT>
-__device__ __noinline__ unsigned slow_select(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
+__device__ __noinline__ SlowPick slow_select(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
                                              const unsigned char* rowp, unsigned* H, unsigned* N, bool bitmaps,
                                              float u) {
   csync();
@@ -1604,11 +1621,14 @@ __device__ __noinline__ unsigned slow_select(const DevCfg& c, const SelArgs& a, 
     }
     if (ok) {
       const LevelPick d = level_pick<DT>(src, sm, mm, Z, draw_target(u, S), true);
-      if (d.ok) return d.idx;
+      if (d.ok) return SlowPick{d.idx, key2f(d.key), mm * kLog2e, true, S};
     }
     restore();
   }
-  return sample_exact(c, src, mm, u, static_cast<unsigned>(a.V), &sm.hist, &sm.red, nullptr, nullptr);
+  unsigned long long S = 0ull;
+  unsigned key = 0u;
+  const unsigned t = sample_exact(c, src, mm, u, static_cast<unsigned>(a.V), &sm.hist, &sm.red, nullptr, &S, &key);
+  return SlowPick{t, key2f(key), mm, false, S};
 }
 
 // ---------------------------------------------------------------------------
@@ -1619,16 +1639,37 @@ __device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddep
 
 // Forced rows do not depend on the logits: the forced ids score 0, all
 // others the filter value; greedy takes the lowest, sampling draws among them.
-__device__ __forceinline__ int forced_token(const DevCfg& c, const RowMeta& rm, int V, float u, bool sample) {
+// *kept = how many equal-scored tokens the step selects from.
+__device__ __forceinline__ int forced_token(const DevCfg& c, const RowMeta& rm, int V, float u, bool sample,
+                                            unsigned long long* kept) {
   int zs[8];
   const int nz = forced_zeros(c, rm, zs);
+  const unsigned long long cnt = nz ? static_cast<unsigned long long>(nz) : static_cast<unsigned long long>(V);
+  *kept = cnt;
   if (!sample) return nz ? zs[0] : 0;
   const unsigned long long W = 1ull << kFixShift;
-  const unsigned long long cnt = nz ? static_cast<unsigned long long>(nz) : static_cast<unsigned long long>(V);
   unsigned long long ncut = cnt;
   if (c.top_p < 1.0f) ncut = group_pick(0ull, W, cnt, topp_target(c.top_p, cnt * W), false);
+  *kept = ncut;
   const unsigned long long nd = group_pick(0ull, W, ncut, draw_target(u, ncut * W), true);
   return nz ? zs[nd - 1] : static_cast<int>(nd - 1);
+}
+
+// Log-probability of a selected token (the log-softmax of the scores the
+// step selects from, at the token): the log of its weight, in the same
+// arithmetic as the weights summed into the kept set's mass S (2^-44 units),
+// less log S.  Fast weights are 2^(fma(s, log2e, -ref)); accurate ones
+// exp(s - ref).  log2 S = its binary exponent plus log2f of its mantissa in
+// [1, 2) (f32 S, 6e-8 relative): no fp64 transcendental, which is slow here.
+__device__ __forceinline__ float token_logprob(float score, float ref, bool fast, unsigned long long S) {
+  constexpr double kLn2 = 0.6931471805599453;
+  const double lnw = fast ? static_cast<double>(fmaf(score, kLog2e, -ref)) * kLn2
+                          : static_cast<double>(score) - static_cast<double>(ref);
+  const unsigned b = __float_as_uint(__ull2float_rn(S));   // S >= 1: a normal float
+  const int e = static_cast<int>(b >> 23) - 127;
+  const float mant = __uint_as_float((b & 0x007fffffu) | 0x3f800000u);
+  const double log2S = static_cast<double>(e - kFixShift) + static_cast<double>(log2f(mant));
+  return static_cast<float>(lnw - log2S * kLn2);
 }
 
 // Block-uniform choice of the sampling threshold from the first sub-chunk's
@@ -1752,10 +1793,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, myrow, a.nrows_total);
       if (rm.bad || rm.L == 0) {
         a.out[myrow] = -1;
+        if (SAMPLE && a.logprobs) a.logprobs[myrow] = __int_as_float(0x7fc00000);   // no token: NaN
         if (rm.bad) atomicOr(c.status, kFlagBadRow);
       } else if (rm.forced) {
         const float u = (SAMPLE && a.uniforms) ? a.uniforms[myrow] : 0.0f;
-        a.out[myrow] = forced_token(c, rm, V, u, SAMPLE);
+        unsigned long long kept = 1ull;
+        a.out[myrow] = forced_token(c, rm, V, u, SAMPLE, &kept);
+        // the kept tokens score equally: each has probability 1 / kept
+        if (SAMPLE && a.logprobs) a.logprobs[myrow] = -logf(static_cast<float>(kept));
       } else {
         streamed = true;
       }
@@ -1918,6 +1963,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     // ---------------- finish the row (all threads) ----------------
     TG_T(row, 2);
     int token = -1;
+    float tok_score = 0.0f, tok_ref = 0.0f;   // sampling: for the log-probability
+    bool tok_fast = true;
+    unsigned long long tok_S = 1ull;
     if (!SAMPLE) {
       // marked tokens, processed exactly, against the best unmarked one
       auto merge = [&](float s, int t) {
@@ -2028,6 +2076,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
           slow = !fr.ok;
           if (slow) reason = fr.reason;
           tok = fr.token;
+          tok_score = fr.score;
+          tok_ref = m * kLog2e;   // the finish weighs 2^(s log2e - m log2e)
+          tok_S = fr.S;
           // Too little candidate mass for the cut or draw: one more pass, read
           // directly (the row is likely still in L2), with a lower threshold.
           // (a draw without top_p that misses its target lies in the bulk of the
@@ -2039,12 +2090,21 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
             slow = !fr2.ok;
             if (slow) reason = 10 + fr2.reason;
             tok = fr2.token;
+            tok_score = fr2.score;
+            tok_S = fr2.S;
           }
         }
       }
       TG_DBG(row, 0, slow ? 1 : 0); TG_DBG(row, 1, reason);
       TG_T(row, 6);
-      if (slow) tok = slow_select<DT>(c, a, sm, rm, rowp, M, N, bitmaps, u);
+      if (slow) {
+        const SlowPick sp = slow_select<DT>(c, a, sm, rm, rowp, M, N, bitmaps, u);
+        tok = sp.token;
+        tok_score = sp.score;
+        tok_ref = sp.ref;
+        tok_fast = sp.fast;
+        tok_S = sp.S;
+      }
       token = static_cast<int>(tok);
     }
 
@@ -2052,6 +2112,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     TG_T(row, 7);
     if (tid == 0) {
       a.out[row] = token;
+      if (SAMPLE && !VERIFY && a.logprobs) a.logprobs[row] = token_logprob(tok_score, tok_ref, tok_fast, tok_S);
       if (VERIFY) {
         // Last of the K+1 positions of row vb counts the matches (steps 4-5).
         const int vb = row / (a.K + 1);

@@ -28,7 +28,7 @@ TG_FLAG_SLOW_PATH = 0x4
 TG_MAX_VOCAB = 1 << 18
 
 # Names of every entry point declared in include/tg.h.
-EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_verify",
+EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
            "tg_status_string", "tg_verify_noalloc")
 TG_NOALLOC_MAX_BATCH = 1024
@@ -90,6 +90,8 @@ def load_library(path: str | None = None):
     lib.tg_config_destroy.argtypes = [c_void_p]
     lib.tg_select.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p]
+    lib.tg_select_logprobs.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_void_p, c_void_p]
     lib.tg_verify.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p]
     lib.tg_verify_noalloc.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, POINTER(tg_params), c_void_p,
@@ -103,7 +105,7 @@ def load_library(path: str | None = None):
     lib.tg_next_num_candidates.restype = c_int32
     lib.tg_status_string.argtypes = [c_int]
     lib.tg_status_string.restype = c_char_p
-    for fn in ("tg_config_create", "tg_config_destroy", "tg_select", "tg_verify", "tg_process",
+    for fn in ("tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify", "tg_process",
                "tg_query_status", "tg_clear_status"):
         getattr(lib, fn).restype = c_int
     _lib = lib
@@ -227,8 +229,10 @@ def _check_len(t, n, name):
         _need(t.numel() >= n, "%s holds %d elements; the call needs %d" % (name, t.numel(), n))
 
 
-def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms, out_ids, stream=None):
-    """logits [B, V]; hist_offsets [B+1]; prompt_lens [B]; uniforms [B] (sampling); out_ids [B].
+def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms, out_ids, stream=None,
+              out_logprobs=None):
+    """logits [B, V]; hist_offsets [B+1]; prompt_lens [B]; uniforms [B] (sampling); out_ids [B];
+    out_logprobs [B] f32 or None (given: tg_select_logprobs, the token's log-probability per row).
     The history ids that hist_offsets point at are not bounds-checked here: they live on the device."""
     import torch
     _need(logits.dim() == 2, "logits must be [B, V]")
@@ -238,13 +242,19 @@ def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms
     _check_len(prompt_lens, B, "prompt_lens")
     _check_len(uniforms, B, "uniforms")
     _check_len(out_ids, B, "out_ids")
-    st = load_library().tg_select(
-        _ptr(logits, "logits", _logit_dtypes()), B, V,
-        _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
-        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
-        cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
-        _ptr(out_ids, "out_ids", (torch.int32,)), _stream(stream))
-    _check("tg_select", st)
+    _check_len(out_logprobs, B, "out_logprobs")
+    args = [_ptr(logits, "logits", _logit_dtypes()), B, V,
+            _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
+            _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+            cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
+            _ptr(out_ids, "out_ids", (torch.int32,))]
+    lib = load_library()
+    if out_logprobs is None:
+        st = lib.tg_select(*args, _stream(stream))
+        _check("tg_select", st)
+    else:
+        st = lib.tg_select_logprobs(*args, _ptr(out_logprobs, "out_logprobs", (torch.float32,)), _stream(stream))
+        _check("tg_select_logprobs", st)
     return out_ids
 
 
