@@ -394,6 +394,58 @@ def processed_scores(x, h, P, p: Params):
 
 
 # ---------------------------------------------------------------------------
+# Beam search, the device part of one step (Transmuter.Generation, module
+# intro, the paragraphs on num_beams; the host's hypotheses are not here)
+# ---------------------------------------------------------------------------
+def log_softmax_row(x: np.ndarray) -> np.ndarray:
+    """The log-softmax of one row of f32 logits: each x_i - logsumexp(x),
+    with the log-sum-exp in fp64, rounded once to f32."""
+    d = x.astype(np.float64)
+    m = d.max()
+    lse = m + np.log(np.sum(np.exp(d - m)))
+    return (d - lse).astype(np.float32)
+
+
+def beam_keep(num_beams: int, p: Params) -> int:
+    """Candidates a prompt keeps per step: max(2, 1 + eos tokens) * num_beams."""
+    return max(2, 1 + len(p.eos_token_ids)) * num_beams
+
+
+def beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams: int, p: Params):
+    """One beam-search step on the device side.
+
+    Rows i*num_beams .. i*num_beams+num_beams-1 are prompt i's beams.  Each
+    row: the log-softmax of its logits, the processors on it (in the order
+    of select), plus the beam's score, in f32, never below the filter value.
+    Of a prompt's num_beams * V candidates (beam b, token t; flat index
+    b*V + t), the best beam_keep() in the order (score desc, flat index asc).
+    Returns (scores [P, K] f32, tokens [P, K] int32, beams [P, K] int32)."""
+    R = len(prompt_lens)
+    assert R % num_beams == 0
+    P = R // num_beams
+    V = p.vocab
+    K = beam_keep(num_beams, p)
+    out_s = np.zeros((P, K), np.float32)
+    out_t = np.zeros((P, K), np.int32)
+    out_b = np.zeros((P, K), np.int32)
+    for i in range(P):
+        cand = np.empty(num_beams * V, np.float32)
+        for b in range(num_beams):
+            r = i * num_beams + b
+            h = hist_ids[int(hist_offsets[r]):int(hist_offsets[r + 1])]
+            x = upcast_row(logits[r], p.logits_dtype)
+            ls = log_softmax_row(x)
+            s, _, _ = process_row(ls, h, int(prompt_lens[r]), p)
+            with np.errstate(over="ignore"):
+                cand[b * V:(b + 1) * V] = _clamp((s + F32(beam_scores[r])).astype(np.float32))
+        flat = order_desc(cand)[:K]
+        out_s[i] = cand[flat]
+        out_t[i] = flat % V
+        out_b[i] = flat // V
+    return out_s, out_t, out_b
+
+
+# ---------------------------------------------------------------------------
 # Assisted generation verify (steps 2-5) and the candidate heuristic (step 6)
 # ---------------------------------------------------------------------------
 def verify(target_logits, cand_ids, K: int, p: Params, uniforms=None):

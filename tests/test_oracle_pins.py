@@ -472,3 +472,88 @@ def test_logprob_forced_and_padding_rows():
     tok, info = O.select_row(x, [1, 2, 5, 6], 1, p, 0.0)
     assert tok == 3 and info.logprob == pytest.approx(-math.log(2), abs=1e-14)
     assert math.isnan(O.select_row(x, [], 0, p, 0.0)[1].logprob)
+
+
+# --------------------------------------------------------------------------
+# beam search, device part of a step (Transmuter.Generation, the paragraphs on
+# num_beams): log-softmax, processors, + beam score, keep max(2, 1 + eos) * beams
+# --------------------------------------------------------------------------
+def test_log_softmax_two_tokens_closed_form():
+    a, b = 1.75, -0.5
+    ls = O.log_softmax_row(np.array([a, b], np.float32))
+    d = b - a
+    assert float(ls[0]) == pytest.approx(-math.log1p(math.exp(d)), abs=2e-7)
+    assert float(ls[1]) == pytest.approx(d - math.log1p(math.exp(d)), abs=2e-7)
+
+
+def test_beam_keep_rule():
+    assert O.beam_keep(4, P(eos_token_ids=[])) == 8
+    assert O.beam_keep(4, P(eos_token_ids=[2])) == 8
+    assert O.beam_keep(3, P(eos_token_ids=[2, 5, 9])) == 12
+
+
+def test_beam_step_brute_force():
+    """Independent: log-softmax with math.fsum / math.log, the candidates of a
+    prompt listed as Python tuples and sorted, flat index split by divmod.
+    The processors are the oracle's own (pinned above)."""
+    rng = np.random.default_rng(21)
+    for trial in range(30):
+        V = int(rng.integers(3, 9))
+        nb = int(rng.integers(1, 4))
+        Pn = int(rng.integers(1, 3))
+        R = Pn * nb
+        eos = [int(rng.integers(0, V))] if rng.random() < 0.7 else []
+        params = P(vocab=V, repetition_penalty=float(rng.choice([1.0, 1.3])), eos_token_ids=eos,
+                   min_length=int(rng.integers(0, 5)), bad_words_ids=[int(rng.integers(0, V))])
+        logits = rng.normal(0, 2, (R, V)).astype(np.float32)
+        hists = [rng.integers(0, V, int(rng.integers(1, 5))).astype(np.int32) for _ in range(R)]
+        off = np.concatenate([[0], np.cumsum([len(h) for h in hists])]).astype(np.int64)
+        ids = np.concatenate(hists).astype(np.int32)
+        plens = np.array([1] * R, np.int32)
+        bs = np.where(rng.random(R) < 0.3, -1e9, rng.normal(-3, 1, R)).astype(np.float32)
+        got_s, got_t, got_b = O.beam_step(logits, bs, ids, off, plens, nb, params)
+        K = max(2, 1 + len(eos)) * nb
+        for i in range(Pn):
+            cands = []
+            for b in range(nb):
+                r = i * nb + b
+                x = [float(v) for v in logits[r]]
+                m = max(x)
+                lse = m + math.log(math.fsum(math.exp(v - m) for v in x))
+                ls = np.array([v - lse for v in x], np.float32)
+                s, _, _ = O.process_row(ls, list(hists[r]), 1, params)
+                for t in range(V):
+                    v = max(float(np.float32(s[t] + bs[r])), float(F))
+                    cands.append((-v, b * V + t))
+            cands.sort()
+            for j in range(K):
+                beam, tok = divmod(cands[j][1], V)
+                assert (int(got_b[i, j]), int(got_t[i, j])) == (beam, tok)
+                assert float(got_s[i, j]) == -cands[j][0]
+
+
+def test_beam_first_step_counts_only_the_first_beam():
+    V, nb = 12, 3
+    x = np.random.default_rng(3).normal(0, 1, V).astype(np.float32)
+    logits = np.stack([x] * nb)
+    bs = np.array([0.0, -1e9, -1e9], np.float32)
+    ids = np.array([1, 1, 1], np.int32)
+    off = np.arange(nb + 1, dtype=np.int64)
+    s, t, b = O.beam_step(logits, bs, ids, off, np.ones(nb, np.int32), nb, P(vocab=V, eos_token_ids=[0]))
+    assert (b == 0).all()
+    assert list(t[0]) == list(np.argsort(-x.astype(np.float64), kind="stable")[:6])
+
+
+def test_beam_repetition_penalty_acts_on_log_probabilities():
+    V = 4
+    x = np.array([2.0, 1.0, 0.5, 3.0], np.float32)
+    ls = O.log_softmax_row(x)
+    s, t, b = O.beam_step(x[None], np.array([-1.0], np.float32), np.array([3], np.int32),
+                          np.array([0, 1], np.int64), np.array([1], np.int32), 1,
+                          P(vocab=V, repetition_penalty=2.0))
+    # log-probabilities are negative: the penalty multiplies the history token's
+    pen = float(np.float32(ls[3] * np.float32(2.0)))
+    assert pen < float(ls[3]) < 0.0
+    assert list(t[0]) == [3, 0]
+    assert float(s[0, 0]) == float(np.float32(np.float32(pen) + np.float32(-1.0)))
+    assert float(s[0, 1]) == float(np.float32(ls[0] + np.float32(-1.0)))
