@@ -38,6 +38,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--beam", action="store_true",
+                    help="time tg_beam_step (64 prompts x 4 beams over the same rows) instead of tg_select")
     ap.add_argument("--logprobs", action="store_true",
                     help="time tg_select_logprobs (ids plus each token's log-probability) instead of tg_select")
     return ap.parse_args()
@@ -343,10 +345,69 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_beam(args):
+    """One beam-search device step over the benchmark rows: 64 prompts x 4 beams."""
+    import numpy as np
+    import torch
+    from logits_processing_token_gb300 import _build
+    _build.build()
+    import logits_processing_token_gb300 as tg
+    from logits_processing_token_gb300 import workloads as W
+
+    w = W.beam_workload()
+    nb = w.extra["beams"]
+    cfg = tg.Config(**w.params)
+    row_bytes = w.B * w.V * 2
+    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / row_bytes)))
+    host_logits = torch.from_numpy(w.logits.view(np.int16))
+    sets = [host_logits.cuda().view(torch.bfloat16) for _ in range(n_sets)]
+    hid = torch.from_numpy(w.hist_ids).cuda()
+    off = torch.from_numpy(w.hist_offsets).cuda()
+    pl = torch.from_numpy(w.prompt_lens).cuda()
+    bs = torch.from_numpy(w.extra["beam_scores"]).cuda()
+    keep = tg.tg_beam_keep(cfg, nb)
+    P = w.B // nb
+    out_s = torch.empty((P, keep), dtype=torch.float32, device="cuda")
+    out_t = torch.empty((P, keep), dtype=torch.int32, device="cuda")
+    out_b = torch.empty((P, keep), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        tg.tg_beam_step(sets[i % n_sets], bs, hid, off, pl, cfg, nb, out_s, out_t, out_b, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    peak, peak_kind = measured_peak()
+    alg = w.B * w.V * 2 + int(w.hist_ids.size) * 4 + w.B * 20
+    achieved = alg / (ms / 1000.0) / 1e9
+    line = {"metric": "beam rows/s (one beam-search device step)", "value": w.B / (ms / 1000.0), "unit": "rows/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "tg_beam_step: %d prompts x %d beams over the benchmark rows, V=151,936 bf16, "
+                                   "full processor chain, keep %d per prompt" % (P, nb, keep),
+                       "l2": "inputs rotate over %d copies of the logits > L2" % n_sets},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                         "bytes_per_launch": alg, "kernel": "beam_kernel<bf16>", "traffic": None},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.beam:
+        run_beam(args)
     else:
         run_ours(args)
 

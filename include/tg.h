@@ -246,6 +246,39 @@ tg_status tg_clear_status(const tg_config* cfg);
  * n_match == K (all candidates matched), else K - 1; bounded to [1, K_max]. */
 int32_t tg_next_num_candidates(int32_t K, int32_t n_match, int32_t K_max);
 
+/*
+ * tg_beam_step -- the device part of one beam-search step
+ * (Transmuter.Generation, module intro, the paragraphs on num_beams; the
+ * host's part -- finished hypotheses, length penalty, stopping -- is the
+ * caller's).
+ *
+ *  logits        device, [num_prompts * num_beams, V], cfg's dtype; prompt i
+ *                owns rows i*num_beams .. i*num_beams + num_beams - 1.
+ *  num_beams     1 .. 8 (one thread-block cluster per prompt).
+ *  beam_scores   device f32 [num_prompts * num_beams]: each beam's running
+ *                score (at the first step 0 for beam 0 and a very negative
+ *                value for the others, so that only the first beam counts).
+ *  hist_ids, hist_offsets, prompt_lens   each beam row's history, as tg_select.
+ *  out_scores    device f32 [num_prompts, keep]; out_tokens, out_beams
+ *                device int32 [num_prompts, keep]; keep = tg_beam_keep().
+ *
+ * Per row: the log-softmax of the logits (f32), the processors of tg_select
+ * in their order (no temperature, top_k or top_p), plus the beam's score, in
+ * f32 and never below the filter value.  Per prompt: the best keep of its
+ * num_beams * V candidates in the order (score desc, beam * V + token asc).
+ * An empty row gives no candidates; a prompt with fewer than keep gets
+ * (filter value, -1, -1) in the remaining slots.  Errors as tg_select;
+ * num_beams outside 1 .. 8 is TG_ERR_UNSUPPORTED.
+ */
+tg_status tg_beam_step(const void* logits, int32_t num_prompts, int32_t num_beams, int32_t V,
+                       const float* beam_scores, const int32_t* hist_ids, const int64_t* hist_offsets,
+                       const int32_t* prompt_lens, const tg_config* cfg, float* out_scores,
+                       int32_t* out_tokens, int32_t* out_beams, tg_stream stream);
+
+/* Candidates a prompt keeps per beam step: max(2, 1 + eos ids) * num_beams,
+ * or -1 for a NULL config or num_beams < 1. */
+int32_t tg_beam_keep(const tg_config* cfg, int32_t num_beams);
+
 /* A static, human-readable name of a status code. */
 const char* tg_status_string(tg_status s);
 

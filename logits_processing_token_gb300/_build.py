@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtg.so")
-SOURCES = ["tg_kernels.cu", "tg_api.cu"]
+SOURCES = ["tg_kernels.cu", "tg_api.cu", "tg_beam.cu"]
 HEADERS = ["tg_device.cuh", os.path.join("..", "..", "include", "tg.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

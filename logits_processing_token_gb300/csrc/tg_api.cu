@@ -329,6 +329,42 @@ tg_status tg_clear_status(const tg_config* cfg) {
   return from_cuda(e);
 }
 
+int32_t tg_beam_keep(const tg_config* cfg, int32_t num_beams) {
+  if (!cfg || num_beams < 1) return -1;
+  const int per = std::max(2, 1 + cfg->dev.n_eos);
+  return per * num_beams;
+}
+
+tg_status tg_beam_step(const void* logits, int32_t num_prompts, int32_t num_beams, int32_t V,
+                       const float* beam_scores, const int32_t* hist_ids, const int64_t* hist_offsets,
+                       const int32_t* prompt_lens, const tg_config* cfg, float* out_scores,
+                       int32_t* out_tokens, int32_t* out_beams, tg_stream stream) {
+  if (!cfg || num_prompts < 0 || num_beams < 1 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
+  if (num_beams > tg::kMaxClusterBeams) return TG_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(num_prompts) * num_beams;
+  if (rows > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return TG_OK;
+  if (!logits || !beam_scores || !hist_offsets || !prompt_lens || !out_scores || !out_tokens || !out_beams)
+    return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  tg::BeamArgs a{};
+  a.logits = logits;
+  a.nrows = static_cast<int>(rows);
+  a.nb = num_beams;
+  a.V = V;
+  a.keep = tg_beam_keep(cfg, num_beams);
+  a.beam_scores = beam_scores;
+  a.hist = hist_ids;
+  a.off = hist_offsets;
+  a.plen = prompt_lens;
+  a.out_scores = out_scores;
+  a.out_tokens = out_tokens;
+  a.out_beams = out_beams;
+  a.nwords = cfg->nwords;
+  return from_cuda(tg::launch_beam(cfg->dev, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int32_t tg_next_num_candidates(int32_t K, int32_t n_match, int32_t K_max) {
   int32_t K2 = n_match >= K ? K + 2 : K - 1;
   if (K_max < 1) K_max = 1;

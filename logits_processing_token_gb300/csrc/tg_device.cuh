@@ -88,6 +88,26 @@ cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, uns
                            int smem, cudaStream_t s);
 cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_sm);
 
+// Beam search, the device part of one step (tg_beam.cu).
+constexpr int kMaxClusterBeams = 8;   // beams of a prompt: one CTA each, one cluster per prompt
+struct BeamArgs {
+  const void* logits;          // [P * nb, V]
+  int nrows;                   // P * nb
+  int nb;                      // beams per prompt
+  int V;
+  int keep;                    // candidates kept per prompt
+  const float* beam_scores;    // [P * nb]
+  const int32_t* hist;
+  const int64_t* off;
+  const int32_t* plen;
+  float* out_scores;           // [P, keep]
+  int32_t* out_tokens;
+  int32_t* out_beams;
+  int nwords;
+};
+int beam_smem_bytes(int nwords);
+cudaError_t launch_beam(const DevCfg& c, const BeamArgs& a, cudaStream_t s);
+
 // ---------------------------------------------------------------------------
 // small helpers
 // ---------------------------------------------------------------------------

@@ -30,7 +30,7 @@ TG_MAX_VOCAB = 1 << 18
 # Names of every entry point declared in include/tg.h.
 EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
-           "tg_status_string", "tg_verify_noalloc")
+           "tg_status_string", "tg_verify_noalloc", "tg_beam_step", "tg_beam_keep")
 TG_NOALLOC_MAX_BATCH = 1024
 
 
@@ -101,6 +101,11 @@ def load_library(path: str | None = None):
                                c_void_p, c_void_p, c_void_p]
     lib.tg_query_status.argtypes = [c_void_p, POINTER(c_uint32), POINTER(c_uint64)]
     lib.tg_clear_status.argtypes = [c_void_p]
+    lib.tg_beam_step.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.tg_beam_step.restype = c_int
+    lib.tg_beam_keep.argtypes = [c_void_p, c_int32]
+    lib.tg_beam_keep.restype = c_int32
     lib.tg_next_num_candidates.argtypes = [c_int32, c_int32, c_int32]
     lib.tg_next_num_candidates.restype = c_int32
     lib.tg_status_string.argtypes = [c_int]
@@ -256,6 +261,40 @@ def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms
         st = lib.tg_select_logprobs(*args, _ptr(out_logprobs, "out_logprobs", (torch.float32,)), _stream(stream))
         _check("tg_select_logprobs", st)
     return out_ids
+
+
+def tg_beam_keep(cfg: Config, num_beams: int) -> int:
+    """Candidates a prompt keeps per beam step: max(2, 1 + eos ids) * num_beams."""
+    n = load_library().tg_beam_keep(cfg.handle, int(num_beams))
+    _need(n > 0, "num_beams must be >= 1")
+    return int(n)
+
+
+def tg_beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, cfg: Config, num_beams: int,
+                 out_scores, out_tokens, out_beams, stream=None):
+    """logits [P * num_beams, V]; beam_scores [P * num_beams] f32; hist_offsets [P * num_beams + 1];
+    prompt_lens [P * num_beams]; out_scores f32, out_tokens and out_beams int32, each [P, keep]."""
+    import torch
+    _need(logits.dim() == 2, "logits must be [P * num_beams, V]")
+    _check_logits(logits, cfg, "logits")
+    R, V = int(logits.shape[0]), int(logits.shape[-1])
+    nb = int(num_beams)
+    _need(nb >= 1 and R % nb == 0, "the rows must be num_beams per prompt")
+    P = R // nb
+    keep = tg_beam_keep(cfg, nb)
+    _check_len(beam_scores, R, "beam_scores")
+    _check_len(hist_offsets, R + 1, "hist_offsets")
+    _check_len(prompt_lens, R, "prompt_lens")
+    for t, name in ((out_scores, "out_scores"), (out_tokens, "out_tokens"), (out_beams, "out_beams")):
+        _check_len(t, P * keep, name)
+    st = load_library().tg_beam_step(
+        _ptr(logits, "logits", _logit_dtypes()), P, nb, V, _ptr(beam_scores, "beam_scores", (torch.float32,)),
+        _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
+        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+        cfg.handle, _ptr(out_scores, "out_scores", (torch.float32,)), _ptr(out_tokens, "out_tokens", (torch.int32,)),
+        _ptr(out_beams, "out_beams", (torch.int32,)), _stream(stream))
+    _check("tg_beam_step", st)
+    return out_scores, out_tokens, out_beams
 
 
 def tg_verify(target_logits, cand_ids, K: int, cfg: Config, uniforms, out_match, out_next, stream=None):

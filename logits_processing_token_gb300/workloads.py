@@ -231,3 +231,22 @@ def random_case(seed: int, B: int, V: int, dtype: str = "f32", mode: str = "samp
     params.update(overrides)
     return Workload("random seed=%d B=%d V=%d %s" % (seed, B, V, dtype), params, logits, ids,
                     off, np.array(plens, np.int32), rng.random(B, dtype=np.float32))
+
+
+def beam_workload(prompts: int = 64, beams: int = 4, V: int = 151_936, seed: int = 1006, L_max: int = 2048,
+                  first_step: bool = False) -> Workload:
+    """A beam-search step over the benchmark workload's rows: prompts * beams
+    rows of its logits, histories and processors (temperature, top_k and top_p
+    do not apply to beam search).  Beam scores are running sums of
+    log-probabilities: N(-12, 3^2) per beam, or (first step) 0 for beam 0 and
+    -1e9 for the others; they and the beam count are in ``extra``."""
+    w = config3(B=prompts * beams, V=V, seed=seed, L_max=L_max)
+    rng = np.random.default_rng(seed + 1)
+    if first_step:
+        bs = np.tile(np.array([0.0] + [-1e9] * (beams - 1), np.float32), prompts)
+    else:
+        bs = (rng.standard_normal(prompts * beams) * 3.0 - 12.0).astype(np.float32)
+    w.name = "beam step %d prompts x %d beams V=%d bf16" % (prompts, beams, V)
+    w.extra["beam_scores"] = bs
+    w.extra["beams"] = beams
+    return w

@@ -429,20 +429,38 @@ def beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beam
     out_t = np.zeros((P, K), np.int32)
     out_b = np.zeros((P, K), np.int32)
     for i in range(P):
-        cand = np.empty(num_beams * V, np.float32)
-        for b in range(num_beams):
-            r = i * num_beams + b
-            h = hist_ids[int(hist_offsets[r]):int(hist_offsets[r + 1])]
-            x = upcast_row(logits[r], p.logits_dtype)
-            ls = log_softmax_row(x)
-            s, _, _ = process_row(ls, h, int(prompt_lens[r]), p)
-            with np.errstate(over="ignore"):
-                cand[b * V:(b + 1) * V] = _clamp((s + F32(beam_scores[r])).astype(np.float32))
-        flat = order_desc(cand)[:K]
-        out_s[i] = cand[flat]
-        out_t[i] = flat % V
-        out_b[i] = flat // V
+        cand, live = beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams, p, i)
+        flat = order_desc(cand)
+        flat = flat[live[flat]][:K]
+        n = flat.size
+        out_s[i, :n] = cand[flat]
+        out_t[i, :n] = flat % V
+        out_b[i, :n] = flat // V
+        # fewer candidates than kept (empty rows give none)
+        out_s[i, n:] = FILTER
+        out_t[i, n:] = -1
+        out_b[i, n:] = -1
     return out_s, out_t, out_b
+
+
+def beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams: int, p: Params, i: int):
+    """Prompt i's num_beams * V candidate scores (flat index b*V + t) and a
+    mask of the live ones (rows with an empty history give none)."""
+    V = p.vocab
+    cand = np.full(num_beams * V, FILTER, np.float32)
+    live = np.zeros(num_beams * V, bool)
+    for b in range(num_beams):
+        r = i * num_beams + b
+        h = hist_ids[int(hist_offsets[r]):int(hist_offsets[r + 1])]
+        if len(h) == 0:
+            continue
+        x = upcast_row(logits[r], p.logits_dtype)
+        ls = log_softmax_row(x)
+        s, _, _ = process_row(ls, h, int(prompt_lens[r]), p)
+        with np.errstate(over="ignore"):
+            cand[b * V:(b + 1) * V] = _clamp((s + F32(beam_scores[r])).astype(np.float32))
+        live[b * V:(b + 1) * V] = True
+    return cand, live
 
 
 # ---------------------------------------------------------------------------

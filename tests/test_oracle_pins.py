@@ -557,3 +557,17 @@ def test_beam_repetition_penalty_acts_on_log_probabilities():
     assert list(t[0]) == [3, 0]
     assert float(s[0, 0]) == float(np.float32(np.float32(pen) + np.float32(-1.0)))
     assert float(s[0, 1]) == float(np.float32(ls[0] + np.float32(-1.0)))
+
+
+def test_beam_empty_rows_give_no_candidates():
+    V, nb = 5, 2
+    x = np.array([[0.5, 1.5, -1.0, 0.0, 2.0]] * 4, np.float32)
+    # prompt 0: beam 0 empty; prompt 1: both empty
+    off = np.array([0, 0, 2, 2, 2], np.int64)
+    ids = np.array([1, 3], np.int32)
+    s, t, b = O.beam_step(x, np.zeros(4, np.float32), ids, off, np.array([0, 1, 0, 0], np.int32), nb,
+                          P(vocab=V, eos_token_ids=[4]))
+    K = 4
+    order = sorted(range(V), key=lambda j: (-float(x[1, j]), j))
+    assert list(b[0]) == [1] * K and list(t[0]) == order[:K]
+    assert list(t[1]) == [-1] * K and list(b[1]) == [-1] * K and all(v == float(F) for v in s[1])
