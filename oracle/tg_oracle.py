@@ -73,7 +73,8 @@ class Params:
     mode: str = "greedy"               # "greedy" or "sample"
     repetition_penalty: float = 1.0
     no_repeat_ngram_size: int = 0
-    bad_words_ids: Sequence[int] = ()  # single-token bad words only
+    bad_words_ids: Sequence[int] = ()  # single-token bad words
+    bad_word_seqs: Sequence[Sequence[int]] = ()   # bad words of one or more tokens
     suppress_tokens: Sequence[int] = ()
     begin_suppress_tokens: Sequence[int] = ()
     eos_token_ids: Sequence[int] = ()
@@ -209,9 +210,16 @@ def process_row(x: np.ndarray, h: Sequence[int], P: int, p: Params):
     for t in ngram_banned_tokens(h, p.no_repeat_ngram_size):
         if 0 <= t < V:
             banned[t] = True
-    # a4 single-token bad_words_ids (a constant mask)
+    # a4 bad_words_ids: a one-token bad word is always banned; a longer one
+    # bans its last token when the row ends with the rest of it
     for t in p.bad_words_ids:
         banned[t] = True
+    hl = [int(t) for t in h]
+    for seq in p.bad_word_seqs:
+        seq = [int(t) for t in seq]
+        n = len(seq)
+        if n == 1 or (L >= n - 1 and hl[L - (n - 1):] == seq[:-1]):
+            banned[seq[-1]] = True
     # a5 min_length / min_new_tokens
     if eos_removed(L, P, p):
         for t in p.eos_token_ids:

@@ -571,3 +571,44 @@ def test_beam_empty_rows_give_no_candidates():
     order = sorted(range(V), key=lambda j: (-float(x[1, j]), j))
     assert list(b[0]) == [1] * K and list(t[0]) == order[:K]
     assert list(t[1]) == [-1] * K and list(b[1]) == [-1] * K and all(v == float(F) for v in s[1])
+
+
+# --------------------------------------------------------------------------
+# a4 with bad words of several tokens (Transmuter.Generation: the bad_words_ids
+# of generation_config.json, one processor in the list of the intro)
+# --------------------------------------------------------------------------
+def test_multi_token_bad_words_hand_cases():
+    V = 12
+    x = np.linspace(1, 2, V).astype(np.float32)
+    p = P(vocab=V, bad_word_seqs=[[3, 4, 5], [7], [9, 10], [2, 6, 11]])
+    # the row ends with 3, 4: bans 5; [7] always; ends with 9? no; [2, 6]? no
+    s, banned, _ = O.process_row(x, [1, 9, 3, 4], 1, p)
+    assert set(np.nonzero(banned)[0].tolist()) == {5, 7}
+    # ends with 9: bans 10
+    s, banned, _ = O.process_row(x, [3, 4, 9], 1, p)
+    assert set(np.nonzero(banned)[0].tolist()) == {7, 10}
+    # prefix longer than the row: nothing but the one-token word
+    s, banned, _ = O.process_row(x, [6], 1, p)
+    assert set(np.nonzero(banned)[0].tolist()) == {7}
+    # ends with 2, 6: bans 11; the banned score is the filter value
+    s, banned, _ = O.process_row(x, [0, 2, 6], 1, p)
+    assert set(np.nonzero(banned)[0].tolist()) == {7, 11} and s[11] == F
+
+
+def test_multi_token_bad_words_against_brute_force():
+    """Independent: the row and each word written as text, one token a
+    bracketed field, compared with str.endswith; random short rows over a
+    tiny vocabulary."""
+    rng = np.random.default_rng(41)
+    for trial in range(200):
+        V = 6
+        words = [list(rng.integers(0, V, int(rng.integers(1, 4)))) for _ in range(int(rng.integers(1, 4)))]
+        h = list(rng.integers(0, V, int(rng.integers(1, 7))))
+        expect = set()
+        row = "".join("<%d>" % t for t in h)
+        for wd in words:
+            # the row's text ends with the word's text without its last token
+            if row.endswith("".join("<%d>" % t for t in wd[:-1])):
+                expect.add(int(wd[-1]))
+        _, banned, _ = O.process_row(np.zeros(V, np.float32), h, 1, P(vocab=V, bad_word_seqs=words))
+        assert set(np.nonzero(banned)[0].tolist()) == expect
