@@ -63,6 +63,7 @@ typedef enum { TG_GREEDY = 0, TG_SAMPLE = 1 } tg_mode;
 /* Largest vocabulary the kernels take. */
 #define TG_MAX_VOCAB (1 << 18)
 /* Longest list accepted for eos ids and forced eos ids. */
+#define TG_MAX_BAD_WORD_LEN 16
 #define TG_MAX_EOS 8
 
 /*
@@ -94,6 +95,14 @@ typedef struct tg_params {
   int32_t top_k;                /* >= 0; 0 = off (sampling only) */
   float top_p;                  /* (0, 1]; 1 = off (sampling only) */
   int32_t max_batch;            /* largest B a tg_verify call may pass; 0 = 4096 */
+  /* Bad words of one or more tokens, back to back: word i is
+   * bad_word_seq_ids[bad_word_seq_offsets[i] .. bad_word_seq_offsets[i+1]),
+   * n_bad_word_seqs + 1 offsets (0 first, non-decreasing), ids in [0, V), each
+   * word at most TG_MAX_BAD_WORD_LEN ids.  A one-token word is always banned;
+   * a longer one bans its last token when the row ends with the rest of it. */
+  const int32_t* bad_word_seq_ids;
+  const int32_t* bad_word_seq_offsets;
+  int32_t n_bad_word_seqs;
 } tg_params;
 
 /* Opaque, immutable after creation; holds the constant masks on the device. */

@@ -125,6 +125,16 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   if (p->top_k < 0) return TG_ERR_INVALID_ARGUMENT;
   if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return TG_ERR_INVALID_ARGUMENT;
   if (p->max_batch < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_bad_word_seqs < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_bad_word_seqs > 0) {
+    if (!p->bad_word_seq_offsets || p->bad_word_seq_offsets[0] != 0) return TG_ERR_INVALID_ARGUMENT;
+    for (int32_t s = 0; s < p->n_bad_word_seqs; ++s) {
+      const int32_t n = p->bad_word_seq_offsets[s + 1] - p->bad_word_seq_offsets[s];
+      if (n < 1 || n > TG_MAX_BAD_WORD_LEN) return TG_ERR_INVALID_ARGUMENT;
+    }
+    if (!ids_in_range(p->bad_word_seq_ids, p->bad_word_seq_offsets[p->n_bad_word_seqs], V))
+      return TG_ERR_INVALID_ARGUMENT;
+  }
 
   tg_config* cfg = new (std::nothrow) tg_config();
   if (!cfg) return TG_ERR_OUT_OF_MEMORY;
@@ -139,20 +149,34 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   cfg->max_batch = p->max_batch ? p->max_batch : 4096;
   cfg->nwords = (V + 31) / 32;
 
-  std::vector<int> ban = sorted_unique({{p->bad_words_ids, p->n_bad_words_ids}, {p->suppress_tokens, p->n_suppress_tokens}});
+  // bad words of one token join the constant ban list; longer ones are kept
+  // as words (ids, then offsets)
+  std::vector<int> one_tok, seq_ids, seq_off{0};
+  for (int32_t s = 0; s < p->n_bad_word_seqs; ++s) {
+    const int32_t o0 = p->bad_word_seq_offsets[s], o1 = p->bad_word_seq_offsets[s + 1];
+    if (o1 - o0 == 1) {
+      one_tok.push_back(p->bad_word_seq_ids[o0]);
+    } else {
+      for (int32_t i = o0; i < o1; ++i) seq_ids.push_back(p->bad_word_seq_ids[i]);
+      seq_off.push_back(static_cast<int>(seq_ids.size()));
+    }
+  }
+  std::vector<int> ban = sorted_unique({{p->bad_words_ids, p->n_bad_words_ids}, {p->suppress_tokens, p->n_suppress_tokens},
+                                        {one_tok.data(), static_cast<int32_t>(one_tok.size())}});
   std::vector<int> sup = sorted_unique({{p->suppress_tokens, p->n_suppress_tokens}});
   std::vector<int> bsup = sorted_unique({{p->begin_suppress_tokens, p->n_begin_suppress_tokens}});
   std::vector<int> feos = sorted_unique({{p->forced_eos_token_ids, p->n_forced_eos_token_ids}});
 
-  // one allocation: [ban][sup][bsup][tickets][status u32][pad][slow_rows u64]
-  const size_t n_int = ban.size() + sup.size() + bsup.size() + static_cast<size_t>(cfg->max_batch) + 2;
+  // one allocation: [ban][sup][bsup][seq ids][seq offsets][tickets][status u32][pad][slow_rows u64]
+  const size_t n_int = ban.size() + sup.size() + bsup.size() + seq_ids.size() + seq_off.size() +
+                       static_cast<size_t>(cfg->max_batch) + 2;
   const size_t bytes = ((n_int * 4 + 15) / 16) * 16 + 16;
   e = cudaMalloc(&cfg->dmem, bytes);
   if (e != cudaSuccess) { delete cfg; return from_cuda(e); }
   std::vector<int> host(bytes / 4, 0);
   size_t o = 0;
   auto put = [&](const std::vector<int>& v) { size_t at = o; std::copy(v.begin(), v.end(), host.begin() + o); o += v.size(); return at; };
-  size_t o_ban = put(ban), o_sup = put(sup), o_bsup = put(bsup);
+  size_t o_ban = put(ban), o_sup = put(sup), o_bsup = put(bsup), o_seq = put(seq_ids), o_soff = put(seq_off);
   size_t o_tick = o; o += cfg->max_batch;
   size_t o_status = o; o += 1;
   size_t o_slow = ((o * 4 + 15) / 16) * 16 / 4;
@@ -170,6 +194,7 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   c.ban_sorted = d + o_ban; c.n_ban = static_cast<int>(ban.size());
   c.sup_sorted = d + o_sup; c.n_sup = static_cast<int>(sup.size());
   c.bsup_sorted = d + o_bsup; c.n_bsup = static_cast<int>(bsup.size());
+  c.seq_ids = d + o_seq; c.seq_off = d + o_soff; c.n_seq = static_cast<int>(seq_off.size()) - 1;
   c.n_eos = p->n_eos_token_ids;
   for (int i = 0; i < c.n_eos; ++i) c.eos[i] = p->eos_token_ids[i];
   c.min_length = p->min_length;

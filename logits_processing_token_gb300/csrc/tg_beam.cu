@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) beam_kernel(const DevCfg c, const
     br.rho = c.rho;
     br.M = M;
     br.N = N;
-    br.bitmaps = !rm.forced && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 ||
+    br.bitmaps = !rm.forced && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
                                 (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
     br.bs = a.beam_scores[r];
     br.lse_hi = 0.0f;

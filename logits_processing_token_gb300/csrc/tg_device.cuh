@@ -45,6 +45,9 @@ struct DevCfg {
   int n_sup;
   const int* bsup_sorted;     // begin-suppress tokens, sorted, unique
   int n_bsup;
+  const int* seq_ids;         // bad words of 2+ tokens, back to back
+  const int* seq_off;         // n_seq + 1 offsets into seq_ids
+  int n_seq;
   int eos[8];
   int n_eos;
   int min_length;
@@ -419,6 +422,14 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
       }
     }
   }
+  // a4, bad words of several tokens: word s bans its last id when the row
+  // ends with its other ids (one-token words are in the constant ban list)
+  for (int s = tid; s < c.n_seq; s += kThreads) {
+    const int o0 = __ldg(c.seq_off + s), o1 = __ldg(c.seq_off + s + 1), k = o1 - o0 - 1;
+    bool hit = L >= k;
+    for (int q = 0; hit && q < k; ++q) hit = hs[L - k + q] == __ldg(c.seq_ids + o0 + q);
+    if (hit) set_bit(N, __ldg(c.seq_ids + o1 - 1));
+  }
   for (int i = tid; i < c.n_ban; i += kThreads) set_bit(N, __ldg(c.ban_sorted + i));
   if (r.eos_off && tid < c.n_eos) set_bit(N, c.eos[tid]);
   if (r.bsup)
@@ -470,6 +481,8 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
   };
   for (int i0 = 0; i0 < L; i0 += kThreads) claim(i0 + tid < L ? hs[i0 + tid] : -1);
   for (int i0 = 0; i0 < c.n_ban; i0 += kThreads) claim(i0 + tid < c.n_ban ? __ldg(c.ban_sorted + i0 + tid) : -1);
+  for (int i0 = 0; i0 < c.n_seq; i0 += kThreads)
+    claim(i0 + tid < c.n_seq ? __ldg(c.seq_ids + __ldg(c.seq_off + i0 + tid + 1) - 1) : -1);
   if (r.eos_off) claim(tid < c.n_eos ? c.eos[tid] : -1);
   if (r.bsup)
     for (int i0 = 0; i0 < c.n_bsup; i0 += kThreads) claim(i0 + tid < c.n_bsup ? __ldg(c.bsup_sorted + i0 + tid) : -1);

@@ -1763,7 +1763,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   const bool tempered = SAMPLE && c.temp != 1.0f;
   // rows take the TMA ring when every row starts on a 16-byte boundary
   const bool tma_ok = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0u) && ((static_cast<size_t>(V) * esz) % 16u == 0u);
-  const bool bitmaps = !VERIFY && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 ||
+  const bool bitmaps = !VERIFY && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
                                    (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
 
   // Inputs may come from the kernel before this one in the stream.

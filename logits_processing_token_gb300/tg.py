@@ -65,6 +65,9 @@ class tg_params(ctypes.Structure):
         ("top_k", c_int32),
         ("top_p", c_float),
         ("max_batch", c_int32),
+        ("bad_word_seq_ids", POINTER(c_int32)),
+        ("bad_word_seq_offsets", POINTER(c_int32)),
+        ("n_bad_word_seqs", c_int32),
     ]
 
 
@@ -136,7 +139,7 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
                 no_repeat_ngram_size=0, bad_words_ids=(), suppress_tokens=(), begin_suppress_tokens=(),
                 eos_token_ids=(), min_length=0, min_new_tokens=0, forced_bos_token_id=-1,
                 forced_eos_token_ids=(), max_new_tokens=0, temperature=1.0, top_k=0, top_p=1.0,
-                max_batch=0):
+                max_batch=0, bad_word_seqs=()):
     """A filled tg_params plus the ctypes arrays its pointers refer to."""
     lib = load_library()
     p = tg_params()
@@ -161,6 +164,19 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
     p.top_k = int(top_k)
     p.top_p = float(top_p)
     p.max_batch = int(max_batch)
+    # bad words of one or more tokens: ids back to back, then n + 1 offsets
+    seqs = [list(map(int, s)) for s in bad_word_seqs]
+    if seqs:
+        flat = [t for s in seqs for t in s]
+        offs = [0]
+        for s in seqs:
+            offs.append(offs[-1] + len(s))
+        ids_arr, _ = _ids(flat)
+        off_arr, _ = _ids(offs)
+        keep += [ids_arr, off_arr]
+        p.bad_word_seq_ids = ctypes.cast(ids_arr, POINTER(c_int32))
+        p.bad_word_seq_offsets = ctypes.cast(off_arr, POINTER(c_int32))
+        p.n_bad_word_seqs = len(seqs)
     return p, keep
 
 

@@ -80,3 +80,13 @@ def test_process_random(seed):
                       repetition_penalty=1.4, no_repeat_ngram_size=2, temperature=0.6, top_k=50, top_p=0.8,
                       eos_token_ids=[1], min_new_tokens=3, suppress_tokens=[4, 5])
     check(w)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_process_multi_token_bad_words(seed):
+    # the rows' ids come from a six-id alphabet, so the words' prefixes match often
+    a = [0, 166, 332, 498, 664, 830]
+    words = [[a[0], a[1], 5], [a[2], 7], [a[5], a[5], a[5], 11], [13], [a[3], a[4], a[0], a[1], 17]]
+    w = W.random_case(40 + seed, B=12, V=997, dtype="f32", mode="sample", L_max=30,
+                      repetition_penalty=1.2, bad_word_seqs=words, bad_words_ids=[19])
+    check(w)

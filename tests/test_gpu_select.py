@@ -178,3 +178,16 @@ def test_nondefault_stream_and_repeat():
     for r in range(w.B):
         if not (infos[r].topp_boundary or infos[r].u_boundary):
             assert ref[r] == ora[r]
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_multi_token_bad_words(mode):
+    a = [0, 166, 332, 498, 664, 830]
+    # the banned last ids score high, so a missed ban changes the selection
+    words = [[a[0], a[1], 5], [a[2], 7], [a[5], a[5], a[5], 11], [13], [a[3], a[4], a[0], 17]]
+    for seed in range(3):
+        w = W.random_case(60 + seed, B=16, V=997, dtype="f32", mode=mode, L_max=30,
+                          repetition_penalty=1.2, bad_word_seqs=words, top_p=0.7)
+        w.logits = w.logits.copy()
+        w.logits[:, [5, 7, 11, 13, 17]] = 30.0
+        compare_select(w, max_boundary_frac=0.34)
