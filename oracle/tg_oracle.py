@@ -508,6 +508,37 @@ def verify(target_logits, cand_ids, K: int, p: Params, uniforms=None):
     return out_match, out_next, infos
 
 
+def verify_history(target_logits, cand_ids, K: int, hist_ids, hist_offsets, prompt_lens, p: Params,
+                   uniforms=None):
+    """tg_verify_history: as verify, but position j of row b runs the whole
+    processor chain with the history the target model saw there -- the row's
+    history followed by its first j candidates (Assisted Generation, "Greedy
+    decoding with assisted generation", step 2: the candidates extend the
+    sequence each position continues).  A row with an empty history is a
+    padding row: no tokens, no matches."""
+    B = target_logits.shape[0]
+    out_match = np.zeros(B, dtype=np.int32)
+    out_next = np.full((B, K + 1), -1, dtype=np.int32)
+    infos = []
+    for b in range(B):
+        h = [int(t) for t in hist_ids[int(hist_offsets[b]):int(hist_offsets[b + 1])]]
+        if not h:
+            infos.append(([-1] * (K + 1), [RowInfo() for _ in range(K + 1)]))
+            continue
+        nxt, row_infos = [], []
+        for j in range(K + 1):
+            x = upcast_row(target_logits[b, j], p.logits_dtype)
+            u = float(uniforms[b, j]) if uniforms is not None else 0.0
+            t, info = select_row(x, h + [int(c) for c in cand_ids[b][:j]], int(prompt_lens[b]), p, u)
+            nxt.append(t)
+            row_infos.append(info)
+        n = matched_prefix(nxt, cand_ids[b], K)
+        out_match[b] = n
+        out_next[b, :n + 1] = nxt[:n + 1]
+        infos.append((nxt, row_infos))
+    return out_match, out_next, infos
+
+
 def matched_prefix(next_tokens: Sequence[int], candidates: Sequence[int], K: int) -> int:
     """Step 4: count matches from the left and stop at the first mismatch;
     later candidates do not count even when they agree."""

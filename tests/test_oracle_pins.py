@@ -612,3 +612,45 @@ def test_multi_token_bad_words_against_brute_force():
                 expect.add(int(wd[-1]))
         _, banned, _ = O.process_row(np.zeros(V, np.float32), h, 1, P(vocab=V, bad_word_seqs=words))
         assert set(np.nonzero(banned)[0].tolist()) == expect
+
+
+# --------------------------------------------------------------------------
+# verify with the processors at every position (Assisted Generation, step 2:
+# each position continues the sequence extended by the earlier candidates)
+# --------------------------------------------------------------------------
+def test_verify_history_without_processors_is_verify():
+    rng = np.random.default_rng(51)
+    B, K, V = 3, 4, 20
+    t = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    cand = rng.integers(0, V, (B, K)).astype(np.int32)
+    ids = np.array([1, 2, 3, 4, 5, 6], np.int32)
+    off = np.array([0, 2, 4, 6], np.int64)
+    pl = np.ones(B, np.int32)
+    a = O.verify(t, cand, K, P(vocab=V))
+    b = O.verify_history(t, cand, K, ids, off, pl, P(vocab=V))
+    assert (a[0] == b[0]).all() and (a[1] == b[1]).all()
+
+
+def test_verify_history_candidates_join_the_history():
+    V, K = 6, 2
+    # every position prefers token 3 by a little; token 3 is the first candidate
+    t = np.zeros((1, K + 1, V), np.float32)
+    t[0, :, 3] = 1.0
+    t[0, :, 4] = 0.5
+    cand = np.array([[3, 3]], np.int32)
+    p = P(vocab=V, repetition_penalty=4.0)
+    m, nxt, _ = O.verify_history(t, cand, K, np.array([0], np.int32), np.array([0, 1], np.int64),
+                                 np.array([1], np.int32), p)
+    # position 0: history [0], 3 wins (match); position 1: history [0, 3] penalises 3 to 0.25 < 0.5
+    assert m[0] == 1 and list(nxt[0]) == [3, 4, -1]
+    # a 2-gram ban that only the first candidate makes
+    p2 = P(vocab=V, no_repeat_ngram_size=2)
+    m2, nxt2, _ = O.verify_history(t, cand, K, np.array([3], np.int32), np.array([0, 1], np.int64),
+                                   np.array([1], np.int32), p2)
+    # position 0: history [3], no earlier (3, x) pair: 3 wins; position 1: [3, 3] ends with 3 and
+    # (3, 3) occurred: 3 is banned, 4 wins
+    assert m2[0] == 1 and list(nxt2[0]) == [3, 4, -1]
+    # an empty history is a padding row
+    m3, nxt3, _ = O.verify_history(t, cand, K, np.array([], np.int32), np.array([0, 0], np.int64),
+                                   np.array([0], np.int32), p)
+    assert m3[0] == 0 and list(nxt3[0]) == [-1, -1, -1]
