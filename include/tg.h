@@ -246,6 +246,22 @@ tg_status tg_verify_noalloc(const void* target_logits, int32_t B, int32_t V, con
                             int32_t K, const tg_params* params, const float* uniforms, int32_t* out_match,
                             int32_t* out_next, tg_stream stream);
 
+/*
+ * tg_verify_history -- tg_verify with the whole processor chain at every
+ * position: position j of row b sees the row's history (hist_ids,
+ * hist_offsets, prompt_lens as tg_select, B rows) followed by its first j
+ * candidates, as the target model did (Assisted Generation, "Greedy decoding
+ * with assisted generation", step 2).  The length rules count that extended
+ * history.  A row with an empty history is a padding row (out_next -1,
+ * out_match 0).  The extended history must fit 8,192 ids: a longer one makes
+ * the position a bad row (-1, status bit).  Other arguments and errors as
+ * tg_verify.
+ */
+tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids, int32_t K,
+                            const int32_t* hist_ids, const int64_t* hist_offsets, const int32_t* prompt_lens,
+                            const tg_config* cfg, const float* uniforms, int32_t* out_match, int32_t* out_next,
+                            tg_stream stream);
+
 /* Read (synchronously) the sticky status bits and the count of rows that took
  * the multi-pass exact path since the last clear. */
 tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_rows);

@@ -6,5 +6,5 @@ from .tg import (  # noqa: F401
     TG_ERR_UNSUPPORTED, TG_FLAG_BAD_ROW, TG_FLAG_HISTORY_ID_OUT_OF_RANGE, TG_FLAG_SLOW_PATH, TG_GREEDY,
     TG_MAX_VOCAB, TG_NOALLOC_MAX_BATCH, TG_OK, TG_SAMPLE, Config, TGError, load_library, make_params, tg_clear_status,
     tg_beam_keep, tg_beam_step, tg_next_num_candidates, tg_params, tg_process, tg_query_status, tg_select,
-    tg_status_string, tg_verify,
+    tg_status_string, tg_verify, tg_verify_history,
 )

@@ -309,6 +309,40 @@ tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32
   return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->ver.smem, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids, int32_t K,
+                            const int32_t* hist_ids, const int64_t* hist_offsets, const int32_t* prompt_lens,
+                            const tg_config* cfg, const float* uniforms, int32_t* out_match, int32_t* out_next,
+                            tg_stream stream) {
+  if (!cfg || B < 0 || V != cfg->V || K < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (B > cfg->max_batch) return TG_ERR_INVALID_ARGUMENT;
+  if (!target_logits || !cand_ids || !out_match || !out_next || !hist_offsets || !prompt_lens)
+    return TG_ERR_INVALID_ARGUMENT;
+  if (cfg->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
+  if (static_cast<long long>(B) * (K + 1) > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  tg::SelArgs a{};
+  a.logits = target_logits;
+  a.nrows = B * (K + 1);
+  a.nrows_total = a.nrows;
+  a.V = V;
+  a.hist = hist_ids;
+  a.off = hist_offsets;
+  a.plen = prompt_lens;
+  a.uniforms = uniforms;
+  a.out = out_next;
+  a.cand = cand_ids;
+  a.K = K;
+  a.out_match = out_match;
+  a.vhist = 1;
+  // the row bitmaps need the select kernel's shared-memory plan
+  a.nstage = cfg->sel.nstage;
+  a.nwords = cfg->nwords;
+  int grid = std::min<long long>(a.nrows, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm);
+  return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
                      const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
                      float* out_scores, uint32_t* out_banbits, float* out_probs, tg_stream stream) {

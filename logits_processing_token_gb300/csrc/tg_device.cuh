@@ -78,6 +78,7 @@ struct SelArgs {
   const int32_t* cand;   // verify
   int K;
   int32_t* out_match;
+  int vhist;             // verify: the processors run at every position, with the candidates as history
   float* logprobs;       // select: the token's log-probability per row, or null
   int nstage;
   int nwords;
@@ -315,12 +316,16 @@ __device__ __forceinline__ unsigned block_max_u(unsigned v, RedScratch* r) {
 struct RowMeta {
   long long h0;     // first history id
   int L, P;
+  int Lb;           // the first Lb ids are hist[h0 ..]; the other L - Lb are ext[0 ..]
+  const int32_t* ext;
   bool bad;         // inconsistent offsets / prompt length
   bool eos_off;     // a5: eos ids removed
   bool forced;      // a6 or a7 active
   bool forced_eos;  // a7 active (it runs after a6 and overrides it)
   bool bsup;        // a9: begin-suppress active
 };
+
+__device__ __forceinline__ void row_meta_rules(const DevCfg& c, RowMeta& r);
 
 // Rows must form a CSR over hist_ids: 0 <= off[b] <= off[b+1] <= off[B].  A
 // row outside that, or with a prompt longer than the row, is flagged bad.
@@ -335,6 +340,14 @@ __device__ __forceinline__ RowMeta row_meta(const DevCfg& c, const int32_t* hist
           (hist == nullptr && L > 0);
   r.L = r.bad ? 0 : static_cast<int>(L);
   r.P = r.bad ? 0 : P;
+  r.Lb = r.L;
+  r.ext = nullptr;
+  row_meta_rules(c, r);
+  return r;
+}
+
+// The length rules of a row whose L and P are set.
+__device__ __forceinline__ void row_meta_rules(const DevCfg& c, RowMeta& r) {
   int Li = r.L, new_tokens = r.L - r.P;
   if (c.min_new > 0) r.eos_off = new_tokens < c.min_new;
   else r.eos_off = c.min_length > 0 && Li < c.min_length;
@@ -343,7 +356,6 @@ __device__ __forceinline__ RowMeta row_meta(const DevCfg& c, const int32_t* hist
   r.forced = fb || r.forced_eos;
   int bidx = (c.bos >= 0 && r.P == 1) ? r.P + 1 : r.P;
   r.bsup = c.n_bsup > 0 && Li == bidx;
-  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -373,14 +385,16 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
   // With a shared-memory stage large enough, the history is copied there
   // first (coalesced, four reads in flight per thread) and every pass below
   // reads shared memory instead of waiting on global loads one at a time.
+  // A row extended by ext (a verify position's candidates) is always staged.
   const bool staged = stage != nullptr && L <= stage_cap;
   if (staged) {
+    const int Lb = r.Lb;
     for (int i0 = 0; i0 < L; i0 += 4 * kThreads) {
       int v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int i = i0 + q * kThreads + tid;
-        v[q] = i < L ? __ldg(h + i) : 0;
+        v[q] = i < L ? (i < Lb ? __ldg(h + i) : __ldg(r.ext + (i - Lb))) : 0;
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {

@@ -1637,6 +1637,46 @@ __device__ __noinline__ SlowPick slow_select(const DevCfg& c, const SelArgs& a, 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Verify position `row` (row b, position j) with the processors: the row's
+// history followed by its first j candidates.  An empty history is a padding
+// row.  The extended history is staged in shared memory, so it must fit the
+// stage (2 * kCandCap ids); a longer one makes the position a bad row.
+__device__ __forceinline__ RowMeta verify_meta(const DevCfg& c, const SelArgs& a, int row) {
+  const int K1 = a.K + 1;
+  const int b = row / K1, j = row % K1;
+  RowMeta r = row_meta(c, a.hist, a.off, a.plen, b, a.nrows_total / K1);
+  if (r.bad || r.L == 0) return r;
+  r.ext = a.cand + static_cast<size_t>(b) * a.K;
+  r.Lb = r.L;
+  r.L += j;
+  if (r.L > 2 * kCandCap) {
+    r.bad = true;
+    r.L = 0;
+    return r;
+  }
+  row_meta_rules(c, r);
+  return r;
+}
+
+// Verify, steps 4-5: the last of a row's K+1 positions to finish counts the
+// left-to-right matches and writes -1 after the first divergent token.  One
+// thread, after writing its position's token.
+__device__ __forceinline__ void verify_ticket(const DevCfg& c, const SelArgs& a, int row) {
+  const int vb = row / (a.K + 1);
+  __threadfence();
+  const unsigned prev = atomicAdd(&c.tickets[vb], 1u);
+  if (prev == static_cast<unsigned>(a.K)) {
+    __threadfence();
+    const int K = a.K;
+    volatile int32_t* nxt = a.out + static_cast<size_t>(vb) * (K + 1);
+    int nm = 0;
+    while (nm < K && nxt[nm] == a.cand[static_cast<size_t>(vb) * K + nm]) ++nm;
+    for (int j = nm + 1; j <= K; ++j) nxt[j] = -1;
+    a.out_match[vb] = nm;
+    c.tickets[vb] = 0u;
+  }
+}
+
 // Forced rows do not depend on the logits: the forced ids score 0, all
 // others the filter value; greedy takes the lowest, sampling draws among them.
 // *kept = how many equal-scored tokens the step selects from.
@@ -1763,7 +1803,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   const bool tempered = SAMPLE && c.temp != 1.0f;
   // rows take the TMA ring when every row starts on a 16-byte boundary
   const bool tma_ok = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0u) && ((static_cast<size_t>(V) * esz) % 16u == 0u);
-  const bool bitmaps = !VERIFY && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
+  const bool bitmaps = (!VERIFY || a.vhist) && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
                                    (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
 
   // Inputs may come from the kernel before this one in the stream.
@@ -1787,20 +1827,22 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   int myrow = 0;
   if (tid < nmine) {
     myrow = a.row_begin + static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x);
-    if (VERIFY) {
+    if (VERIFY && !a.vhist) {
       streamed = true;
     } else {
-      const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, myrow, a.nrows_total);
+      const RowMeta rm = VERIFY ? verify_meta(c, a, myrow) : row_meta(c, a.hist, a.off, a.plen, myrow, a.nrows_total);
       if (rm.bad || rm.L == 0) {
         a.out[myrow] = -1;
-        if (SAMPLE && a.logprobs) a.logprobs[myrow] = __int_as_float(0x7fc00000);   // no token: NaN
+        if (!VERIFY && SAMPLE && a.logprobs) a.logprobs[myrow] = __int_as_float(0x7fc00000);   // no token: NaN
         if (rm.bad) atomicOr(c.status, kFlagBadRow);
+        if (VERIFY) verify_ticket(c, a, myrow);
       } else if (rm.forced) {
         const float u = (SAMPLE && a.uniforms) ? a.uniforms[myrow] : 0.0f;
         unsigned long long kept = 1ull;
         a.out[myrow] = forced_token(c, rm, V, u, SAMPLE, &kept);
         // the kept tokens score equally: each has probability 1 / kept
-        if (SAMPLE && a.logprobs) a.logprobs[myrow] = -logf(static_cast<float>(kept));
+        if (!VERIFY && SAMPLE && a.logprobs) a.logprobs[myrow] = -logf(static_cast<float>(kept));
+        if (VERIFY) verify_ticket(c, a, myrow);
       } else {
         streamed = true;
       }
@@ -1844,8 +1886,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     const int row = sm.rows[ri];
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
     RowMeta rm;
-    if (VERIFY) {
-      rm.bad = false; rm.L = 1; rm.P = 0; rm.h0 = 0;
+    if (VERIFY && a.vhist) {
+      rm = verify_meta(c, a, row);
+    } else if (VERIFY) {
+      rm.bad = false; rm.L = 1; rm.P = 0; rm.h0 = 0; rm.Lb = 1; rm.ext = nullptr;
       rm.eos_off = rm.forced = rm.forced_eos = rm.bsup = false;
     } else {
       rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
@@ -2113,22 +2157,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     if (tid == 0) {
       a.out[row] = token;
       if (SAMPLE && !VERIFY && a.logprobs) a.logprobs[row] = token_logprob(tok_score, tok_ref, tok_fast, tok_S);
-      if (VERIFY) {
-        // Last of the K+1 positions of row vb counts the matches (steps 4-5).
-        const int vb = row / (a.K + 1);
-        __threadfence();
-        const unsigned prev = atomicAdd(&c.tickets[vb], 1u);
-        if (prev == static_cast<unsigned>(a.K)) {
-          __threadfence();
-          const int K = a.K;
-          volatile int32_t* nxt = a.out + static_cast<size_t>(vb) * (K + 1);
-          int nm = 0;
-          while (nm < K && nxt[nm] == a.cand[static_cast<size_t>(vb) * K + nm]) ++nm;
-          for (int j = nm + 1; j <= K; ++j) nxt[j] = -1;
-          a.out_match[vb] = nm;
-          c.tickets[vb] = 0u;
-        }
-      }
+      if (VERIFY) verify_ticket(c, a, row);
     }
     csync();
   }

@@ -30,7 +30,8 @@ TG_MAX_VOCAB = 1 << 18
 # Names of every entry point declared in include/tg.h.
 EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
-           "tg_status_string", "tg_verify_noalloc", "tg_beam_step", "tg_beam_keep")
+           "tg_status_string", "tg_verify_noalloc", "tg_beam_step", "tg_beam_keep",
+           "tg_verify_history")
 TG_NOALLOC_MAX_BATCH = 1024
 
 
@@ -97,6 +98,9 @@ def load_library(path: str | None = None):
                                        c_void_p, c_void_p, c_void_p]
     lib.tg_verify.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p]
+    lib.tg_verify_history.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.tg_verify_history.restype = c_int
     lib.tg_verify_noalloc.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, POINTER(tg_params), c_void_p,
                                       c_void_p, c_void_p, c_void_p]
     lib.tg_verify_noalloc.restype = c_int
@@ -330,6 +334,32 @@ def tg_verify(target_logits, cand_ids, K: int, cfg: Config, uniforms, out_match,
         int(K), cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
         _ptr(out_match, "out_match", (torch.int32,)), _ptr(out_next, "out_next", (torch.int32,)), _stream(stream))
     _check("tg_verify", st)
+    return out_match, out_next
+
+
+def tg_verify_history(target_logits, cand_ids, K: int, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms,
+                      out_match, out_next, stream=None):
+    """tg_verify with the processors at every position: position j of row b sees
+    the row's history (hist_offsets [B+1], prompt_lens [B]) and its first j candidates."""
+    import torch
+    _need(target_logits.dim() == 3 and int(target_logits.shape[1]) == int(K) + 1,
+          "target_logits must be [B, K+1, V]")
+    _check_logits(target_logits, cfg, "target_logits")
+    B, V = int(target_logits.shape[0]), int(target_logits.shape[-1])
+    _check_len(cand_ids, B * int(K), "cand_ids")
+    _check_len(hist_offsets, B + 1, "hist_offsets")
+    _check_len(prompt_lens, B, "prompt_lens")
+    _check_len(uniforms, B * (int(K) + 1), "uniforms")
+    _check_len(out_match, B, "out_match")
+    _check_len(out_next, B * (int(K) + 1), "out_next")
+    st = load_library().tg_verify_history(
+        _ptr(target_logits, "target_logits", _logit_dtypes()), B, V, _ptr(cand_ids, "cand_ids", (torch.int32,)),
+        int(K),
+        _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
+        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+        cfg.handle, _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True),
+        _ptr(out_match, "out_match", (torch.int32,)), _ptr(out_next, "out_next", (torch.int32,)), _stream(stream))
+    _check("tg_verify_history", st)
     return out_match, out_next
 
 

@@ -81,3 +81,58 @@ def test_candidate_heuristic_trace():
         trace.append(K2)
         K = K2
     assert trace[:2] == [7, 9]
+
+
+def run_gpu_history(w, tgt, cand, K, hists, plens):
+    import torch
+    import logits_processing_token_gb300 as tg
+    cfg = tg.Config(**w.params, max_batch=64)
+    ids, off = W._pack([np.asarray(h, np.int32) for h in hists])
+    t = torch.from_numpy(np.ascontiguousarray(tgt)).cuda()
+    c = torch.from_numpy(cand).cuda()
+    u = torch.from_numpy(np.ascontiguousarray(w.uniforms)).cuda()
+    om = torch.full((w.B,), -9, dtype=torch.int32, device="cuda")
+    on = torch.full((w.B, K + 1), -9, dtype=torch.int32, device="cuda")
+    tg.tg_verify_history(t, c, K, torch.from_numpy(ids).cuda(), torch.from_numpy(off).cuda(),
+                         torch.from_numpy(np.asarray(plens, np.int32)).cuda(), cfg, u, om, on)
+    torch.cuda.synchronize()
+    return om.cpu().numpy(), on.cpu().numpy(), ids, off
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+@pytest.mark.parametrize("K", [1, 5, 16])
+def test_verify_history_parity(mode, K):
+    """Processors at every position with the candidates as history: repetition
+    penalty, 3-gram bans, bad words of several tokens, min_new_tokens, forced
+    eos, against the oracle's verify_history."""
+    B = 12
+    w, tgt, cand, _ = make_case(B, K, mode, repetition_penalty=1.5, no_repeat_ngram_size=3,
+                                eos_token_ids=[2], min_new_tokens=4, forced_eos_token_ids=[2], max_new_tokens=9,
+                                bad_word_seqs=[[5, 9], [17, 23, 31]])
+    rng = np.random.default_rng(100 + K)
+    hists, plens = [], []
+    for b in range(B):
+        if b == 3:
+            hists.append([])          # a padding row
+            plens.append(0)
+            continue
+        L = int(rng.integers(1, 40))
+        h = list(rng.integers(0, 50, L))
+        # repeat the first candidates inside the history so penalties and n-grams fire
+        h[:2] = [int(cand[b, 0]), int(cand[b, min(1, K - 1)])]
+        hists.append(h)
+        plens.append(int(rng.integers(1, L + 1)))
+    om, on, ids, off = run_gpu_history(w, tgt, cand, K, hists, plens)
+    p = O.Params(**w.params)
+    m_ref, n_ref, infos = O.verify_history(tgt, cand, K, ids, off, np.asarray(plens, np.int32), p, w.uniforms)
+    checked = 0
+    for b in range(B):
+        nxt, row_infos = infos[b]
+        upto = int(m_ref[b])
+        if any(ri.u_boundary or ri.topp_boundary for ri in row_infos[:upto + 1]):
+            continue
+        assert om[b] == m_ref[b], (b, om[b], m_ref[b])
+        assert list(on[b]) == list(n_ref[b]), (b, on[b], n_ref[b])
+        checked += 1
+    assert checked >= B - 3
+    assert om[3] == 0 and list(on[3]) == [-1] * (K + 1)
