@@ -86,6 +86,7 @@ class Params:
     temperature: float = 1.0
     top_k: int = 0
     top_p: float = 1.0
+    renormalize_logits: bool = False   # log-softmax after the processors (diagnostic scores, beam step)
 
 
 @dataclass
@@ -358,7 +359,11 @@ def selected_from_scores(s_t: np.ndarray, order: np.ndarray, n_kept: int, s_k: n
 
 def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float):
     """One row of tg_select.  Returns (token id or -1, RowInfo); the info
-    carries the token's log-probability (NaN for a padding row)."""
+    carries the token's log-probability (NaN for a padding row).
+
+    renormalize_logits shifts a row's scores by one constant; argmax,
+    temperature, top_k, top_p, the draw and the log-probability do not change
+    under it (exactly, before rounding), so selection leaves it out."""
     if len(h) == 0:
         return -1, RowInfo()
     s, _, info = process_row(x, h, P, p)
@@ -396,6 +401,8 @@ def processed_scores(x, h, P, p: Params):
     """What the diagnostic entry point writes: scores after a0-a9 (greedy) or
     a0-a10 (sampling), and the mask of banned tokens."""
     s, banned, _ = process_row(x, h, P, p)
+    if p.renormalize_logits:
+        s = _clamp(log_softmax_row(s))
     if p.mode == "sample":
         s = apply_temperature(s, p)
     return s, banned
@@ -465,6 +472,8 @@ def beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, nu
         x = upcast_row(logits[r], p.logits_dtype)
         ls = log_softmax_row(x)
         s, _, _ = process_row(ls, h, int(prompt_lens[r]), p)
+        if p.renormalize_logits:
+            s = _clamp(log_softmax_row(s))
         with np.errstate(over="ignore"):
             cand[b * V:(b + 1) * V] = _clamp((s + F32(beam_scores[r])).astype(np.float32))
         live[b * V:(b + 1) * V] = True

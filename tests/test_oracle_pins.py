@@ -654,3 +654,29 @@ def test_verify_history_candidates_join_the_history():
     m3, nxt3, _ = O.verify_history(t, cand, K, np.array([], np.int32), np.array([0, 0], np.int64),
                                    np.array([0], np.int32), p)
     assert m3[0] == 0 and list(nxt3[0]) == [-1, -1, -1]
+
+
+# --------------------------------------------------------------------------
+# renormalize_logits (Transmuter.Generation intro: after the task's
+# processors, before temperature): a log-softmax of the processed scores
+# --------------------------------------------------------------------------
+def test_renormalize_logits_is_a_normalised_shift():
+    rng = np.random.default_rng(61)
+    V = 40
+    x = rng.normal(0, 3, V).astype(np.float32)
+    p = P(vocab=V, repetition_penalty=1.3, suppress_tokens=[3, 4], renormalize_logits=True)
+    s, banned = O.processed_scores(x, [1, 2, 5], 1, p)
+    s0, _ = O.processed_scores(x, [1, 2, 5], 1, P(vocab=V, repetition_penalty=1.3, suppress_tokens=[3, 4]))
+    keep = ~banned
+    # probabilities sum to one (math.fsum), removed tokens stay removed
+    assert math.fsum(math.exp(float(v)) for v in s[keep]) == pytest.approx(1.0, abs=1e-6)
+    assert (s[banned] == F).all()
+    # the same shift for every kept token: log-sum-exp of the unnormalised scores
+    lse = math.log(math.fsum(math.exp(float(v)) for v in s0[keep]))
+    assert np.allclose(s[keep].astype(np.float64), s0[keep].astype(np.float64) - lse, atol=2e-6)
+    # selection is unchanged by it
+    for mode in ("greedy", "sample"):
+        for u in (0.1, 0.5, 0.9):
+            a = O.select_row(x, [1, 2, 5], 1, P(vocab=V, mode=mode, renormalize_logits=True, top_p=0.8), u)
+            b = O.select_row(x, [1, 2, 5], 1, P(vocab=V, mode=mode, top_p=0.8), u)
+            assert a[0] == b[0]
