@@ -103,6 +103,11 @@ typedef struct tg_params {
   const int32_t* bad_word_seq_ids;
   const int32_t* bad_word_seq_offsets;
   int32_t n_bad_word_seqs;
+  /* 0/1: renormalize_logits, a log-softmax of the scores after the processors
+   * and before temperature.  Selection does not change under it (a per-row
+   * shift); tg_process applies it; tg_beam_step does not take it yet
+   * (TG_ERR_UNSUPPORTED). */
+  int32_t renormalize_logits;
 } tg_params;
 
 /* Opaque, immutable after creation; holds the constant masks on the device. */

@@ -195,6 +195,7 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   c.sup_sorted = d + o_sup; c.n_sup = static_cast<int>(sup.size());
   c.bsup_sorted = d + o_bsup; c.n_bsup = static_cast<int>(bsup.size());
   c.seq_ids = d + o_seq; c.seq_off = d + o_soff; c.n_seq = static_cast<int>(seq_off.size()) - 1;
+  c.renorm = p->renormalize_logits ? 1 : 0;
   c.n_eos = p->n_eos_token_ids;
   for (int i = 0; i < c.n_eos; ++i) c.eos[i] = p->eos_token_ids[i];
   c.min_length = p->min_length;
@@ -399,7 +400,7 @@ tg_status tg_beam_step(const void* logits, int32_t num_prompts, int32_t num_beam
                        const int32_t* prompt_lens, const tg_config* cfg, float* out_scores,
                        int32_t* out_tokens, int32_t* out_beams, tg_stream stream) {
   if (!cfg || num_prompts < 0 || num_beams < 1 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
-  if (num_beams > tg::kMaxClusterBeams) return TG_ERR_UNSUPPORTED;
+  if (num_beams > tg::kMaxClusterBeams || cfg->dev.renorm) return TG_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(num_prompts) * num_beams;
   if (rows > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
   if (rows == 0) return TG_OK;

@@ -48,6 +48,7 @@ struct DevCfg {
   const int* seq_ids;         // bad words of 2+ tokens, back to back
   const int* seq_off;         // n_seq + 1 offsets into seq_ids
   int n_seq;
+  int renorm;                 // renormalize_logits
   int eos[8];
   int n_eos;
   int min_length;

@@ -2221,8 +2221,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                            : __uint_as_float(static_cast<unsigned>(__ldg(static_cast<const unsigned short*>(rowp) + i)) << 16);
       s = process_elem(c, H, N, x, i, false);
     }
-    if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
+    if (!c.renorm && sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
     sc[i] = s;
+  }
+  if (c.renorm) {
+    // renormalize_logits: s - logsumexp(s), the log-sum-exp as hi + lo (ln S
+    // from S's exponent and log2f of its mantissa), then temperature
+    csync();
+    float tm = -INFINITY;
+    for (int i = threadIdx.x; i < V; i += kThreads) tm = fmaxf(tm, sc[i]);
+    const float m = block_max(tm, &sm.red);
+    float ts = 0.0f;
+    for (int i = threadIdx.x; i < V; i += kThreads) ts += expf(sc[i] - m);
+    const float S = block_sum_f(ts, &sm.red);
+    constexpr double kLn2 = 0.6931471805599453;
+    const unsigned b = __float_as_uint(S);
+    const int e = static_cast<int>(b >> 23) - 127;
+    const float mant = __uint_as_float((b & 0x007fffffu) | 0x3f800000u);
+    const double lse = static_cast<double>(m) + (static_cast<double>(e) + static_cast<double>(log2f(mant))) * kLn2;
+    const float hi = static_cast<float>(lse), lo = static_cast<float>(lse - static_cast<double>(hi));
+    for (int i = threadIdx.x; i < V; i += kThreads) {
+      float s = clampf(__fsub_rn(__fsub_rn(sc[i], hi), lo));
+      if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
+      sc[i] = s;
+    }
   }
   if (out_banbits) {
     unsigned* bb = out_banbits + static_cast<size_t>(row) * a.nwords;

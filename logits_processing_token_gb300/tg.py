@@ -69,6 +69,7 @@ class tg_params(ctypes.Structure):
         ("bad_word_seq_ids", POINTER(c_int32)),
         ("bad_word_seq_offsets", POINTER(c_int32)),
         ("n_bad_word_seqs", c_int32),
+        ("renormalize_logits", c_int32),
     ]
 
 
@@ -143,7 +144,7 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
                 no_repeat_ngram_size=0, bad_words_ids=(), suppress_tokens=(), begin_suppress_tokens=(),
                 eos_token_ids=(), min_length=0, min_new_tokens=0, forced_bos_token_id=-1,
                 forced_eos_token_ids=(), max_new_tokens=0, temperature=1.0, top_k=0, top_p=1.0,
-                max_batch=0, bad_word_seqs=()):
+                max_batch=0, bad_word_seqs=(), renormalize_logits=False):
     """A filled tg_params plus the ctypes arrays its pointers refer to."""
     lib = load_library()
     p = tg_params()
@@ -168,6 +169,7 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
     p.top_k = int(top_k)
     p.top_p = float(top_p)
     p.max_batch = int(max_batch)
+    p.renormalize_logits = 1 if renormalize_logits else 0
     # bad words of one or more tokens: ids back to back, then n + 1 offsets
     seqs = [list(map(int, s)) for s in bad_word_seqs]
     if seqs:

@@ -90,3 +90,40 @@ def test_process_multi_token_bad_words(seed):
     w = W.random_case(40 + seed, B=12, V=997, dtype="f32", mode="sample", L_max=30,
                       repetition_penalty=1.2, bad_word_seqs=words, bad_words_ids=[19])
     check(w)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_process_renormalize_logits(mode):
+    """renormalize_logits: the scores after the processors less their
+    log-sum-exp (before temperature).  The kernel forms s - lse with lse as a
+    two-float pair, the oracle rounds s - lse once from fp64: a few ulp apart,
+    2e-6 * max(1, |s|); removed tokens stay at the filter value bit for bit."""
+    w = W.random_case(70, B=8, V=997, dtype="f32", mode=mode, repetition_penalty=1.3, suppress_tokens=[4, 5],
+                      temperature=0.7, renormalize_logits=True)
+    sc, bb, pr = run_process(w)
+    p = O.Params(**w.params)
+    for b in range(w.B):
+        h = list(w.history(b))
+        if not h:
+            continue
+        x = O.upcast_row(w.logits[b], p.logits_dtype)
+        s_ref, banned = O.processed_scores(x, h, int(w.prompt_lens[b]), p)
+        d = np.abs(sc[b].astype(np.float64) - s_ref.astype(np.float64))
+        assert np.all(d <= 2e-6 * np.maximum(1.0, np.abs(s_ref.astype(np.float64)))), (b, d.max())
+        assert np.array_equal(sc[b][banned], s_ref[banned])
+
+
+def test_beam_step_rejects_renormalize():
+    import torch
+    import logits_processing_token_gb300 as tg
+    cfg = tg.Config(vocab=64, renormalize_logits=True)
+    x = torch.zeros((2, 64), device="cuda")
+    z = torch.zeros(2, device="cuda")
+    off = torch.tensor([0, 1, 2], dtype=torch.int64, device="cuda")
+    ids = torch.tensor([1, 2], dtype=torch.int32, device="cuda")
+    pl = torch.ones(2, dtype=torch.int32, device="cuda")
+    keep = tg.tg_beam_keep(cfg, 2)
+    s = torch.zeros((1, keep), device="cuda")
+    t = torch.zeros((1, keep), dtype=torch.int32, device="cuda")
+    with pytest.raises(tg.TGError):
+        tg.tg_beam_step(x, z, ids, off, pl, cfg, 2, s, t, t.clone())
