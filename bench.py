@@ -52,6 +52,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device):
+    """The largest of one float over all ranks (every rank gets it); the step
+    time of a multi-GPU run is the slowest rank's."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, rows_per_rank, ms_per_step):
+    """Rows per second over all ranks: every rank selects its own rows."""
+    return world * rows_per_rank / (ms_per_step / 1000.0)
+
+
 CSRC = os.path.join(ROOT, "logits_processing_token_gb300", "csrc")
 PROFILE = os.path.join(ROOT, "profiles", "select_kernel_bf16_workload3.md")
 
@@ -261,12 +278,9 @@ def run_ours(args):
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
     flags, slow_rows = tg.tg_query_status(cfg)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / K
-    value = world * B / (ms_per_step / 1000.0)
+    value = whole_job_rate(world, B, ms_per_step)
 
     alg_bytes, n_read = required_bytes(w)
     # one select_kernel launch per step (B <= 512 rows per CTA): its average
@@ -330,11 +344,8 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        line["e2e"] = {"value": world * B / (e_ms / 1000.0), "unit": "rows/s", "h2d_bytes_per_step": bi,
+        e_ms = max_over_ranks(e_ms, world, "cuda")
+        line["e2e"] = {"value": whole_job_rate(world, B, e_ms), "unit": "rows/s", "h2d_bytes_per_step": bi,
                        "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
