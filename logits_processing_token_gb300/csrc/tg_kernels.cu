@@ -1784,8 +1784,12 @@ __device__ __forceinline__ RowSums block_row_sums(SelSmem& sm, unsigned long lon
   return r;
 }
 
-template <int DT, bool VERIFY, bool SAMPLE>
+// VMODE: 0 select, 1 verify, 2 verify with the processors at every position
+// (a compile-time choice, so plain verify carries none of the bitmap code).
+template <int DT, int VMODE, bool SAMPLE>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, const SelArgs a) {
+  constexpr bool VERIFY = VMODE != 0;
+  constexpr bool VHIST = VMODE == 2;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   unsigned* M = reinterpret_cast<unsigned*>(smem_raw + fin_offset());   // marked (history | banned)
@@ -1803,7 +1807,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   const bool tempered = SAMPLE && c.temp != 1.0f;
   // rows take the TMA ring when every row starts on a 16-byte boundary
   const bool tma_ok = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0u) && ((static_cast<size_t>(V) * esz) % 16u == 0u);
-  const bool bitmaps = (!VERIFY || a.vhist) && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
+  const bool bitmaps = (!VERIFY || VHIST) && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
                                    (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
 
   // Inputs may come from the kernel before this one in the stream.
@@ -1827,7 +1831,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   int myrow = 0;
   if (tid < nmine) {
     myrow = a.row_begin + static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x);
-    if (VERIFY && !a.vhist) {
+    if (VERIFY && !VHIST) {
       streamed = true;
     } else {
       const RowMeta rm = VERIFY ? verify_meta(c, a, myrow) : row_meta(c, a.hist, a.off, a.plen, myrow, a.nrows_total);
@@ -1886,7 +1890,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     const int row = sm.rows[ri];
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
     RowMeta rm;
-    if (VERIFY && a.vhist) {
+    if (VERIFY && VHIST) {
       rm = verify_meta(c, a, row);
     } else if (VERIFY) {
       rm.bad = false; rm.L = 1; rm.P = 0; rm.h0 = 0; rm.Lb = 1; rm.ext = nullptr;
@@ -2417,9 +2421,9 @@ int process_smem_bytes(int nwords) {
 // One launch per kMaxRowsPerCta * grid rows; each is a programmatic dependent
 // of the kernel before it in the stream (its launch overlaps that kernel's
 // tail; it waits for it before touching global memory).
-template <int DT, bool VERIFY, bool SAMPLE>
+template <int DT, int VMODE, bool SAMPLE>
 static cudaError_t launch_sel(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s) {
-  auto k = select_kernel<DT, VERIFY, SAMPLE>;
+  auto k = select_kernel<DT, VMODE, SAMPLE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -2443,15 +2447,20 @@ static cudaError_t launch_sel(const DevCfg& c, const SelArgs& a, int grid, int s
   return cudaGetLastError();
 }
 
-template <int DT, bool VERIFY>
+template <int DT, int VMODE>
 static cudaError_t launch_sel_m(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s) {
-  return c.mode == kSample ? launch_sel<DT, VERIFY, true>(c, a, grid, smem, s) : launch_sel<DT, VERIFY, false>(c, a, grid, smem, s);
+  return c.mode == kSample ? launch_sel<DT, VMODE, true>(c, a, grid, smem, s) : launch_sel<DT, VMODE, false>(c, a, grid, smem, s);
+}
+
+template <int DT>
+static cudaError_t launch_sel_v(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s) {
+  if (!verify) return launch_sel_m<DT, 0>(c, a, grid, smem, s);
+  return a.vhist ? launch_sel_m<DT, 2>(c, a, grid, smem, s) : launch_sel_m<DT, 1>(c, a, grid, smem, s);
 }
 
 cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s) {
   if (a.nstage < 2 || a.nstage > kMaxStages || grid < 1) return cudaErrorInvalidValue;
-  if (c.dtype == kF32) return verify ? launch_sel_m<kF32, true>(c, a, grid, smem, s) : launch_sel_m<kF32, false>(c, a, grid, smem, s);
-  return verify ? launch_sel_m<kBF16, true>(c, a, grid, smem, s) : launch_sel_m<kBF16, false>(c, a, grid, smem, s);
+  return c.dtype == kF32 ? launch_sel_v<kF32>(c, a, verify, grid, smem, s) : launch_sel_v<kBF16>(c, a, verify, grid, smem, s);
 }
 
 cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
@@ -2474,10 +2483,10 @@ cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_s
   int worst = 1 << 20;
   for (int t = 0; t < 2; ++t) {
     void (*k)(DevCfg, SelArgs);
-    if (dtype == kF32) k = verify ? (t ? select_kernel<kF32, true, true> : select_kernel<kF32, true, false>)
-                                  : (t ? select_kernel<kF32, false, true> : select_kernel<kF32, false, false>);
-    else k = verify ? (t ? select_kernel<kBF16, true, true> : select_kernel<kBF16, true, false>)
-                    : (t ? select_kernel<kBF16, false, true> : select_kernel<kBF16, false, false>);
+    if (dtype == kF32) k = verify ? (t ? select_kernel<kF32, 1, true> : select_kernel<kF32, 1, false>)
+                                  : (t ? select_kernel<kF32, 0, true> : select_kernel<kF32, 0, false>);
+    else k = verify ? (t ? select_kernel<kBF16, 1, true> : select_kernel<kBF16, 1, false>)
+                    : (t ? select_kernel<kBF16, 0, true> : select_kernel<kBF16, 0, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int occ = 0;
