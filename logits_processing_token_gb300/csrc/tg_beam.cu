@@ -6,7 +6,7 @@
 // The host's part of the step (finished hypotheses, length penalty,
 // stopping) is not here.
 //
-// One thread-block cluster per prompt, one CTA (16 warps) per beam row.  A
+// One thread-block cluster per prompt, one CTA (8 warps) per beam row.  A
 // CTA reads its row once for the log-sum-exp, then selects its own best keep
 // candidates with the radix k-th-key engine over the processed scores (the
 // row is in L2 by then); after a cluster barrier, CTA 0 of the cluster reads
@@ -17,6 +17,9 @@
 
 #include <cuda_runtime.h>
 
+// 8 warps per beam row: two CTAs share an SM, so a step's clusters run in
+// one wave and one CTA's barriers overlap the other's passes
+#define TG_THREADS 256
 #include "../../include/tg.h"
 #include "tg_device.cuh"
 
@@ -211,7 +214,7 @@ struct BeamScores {
 };
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) beam_kernel(const DevCfg c, const BeamArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) beam_kernel(const DevCfg c, const BeamArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BeamSmem& sm = *reinterpret_cast<BeamSmem*>(smem_raw);
   unsigned* M = reinterpret_cast<unsigned*>(smem_raw + kBeamFixed);

@@ -12,7 +12,13 @@
 
 namespace tg {
 
-constexpr int kThreads = 512;               // threads per CTA of every kernel
+// Threads per CTA: 512 for every kernel of tg_kernels.cu; a translation unit
+// may define TG_THREADS before including this header (tg_beam.cu: 256, two
+// CTAs per SM).
+#ifndef TG_THREADS
+#define TG_THREADS 512
+#endif
+constexpr int kThreads = TG_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStageBytes = 32768;          // one TMA bulk copy / sub-chunk of a row
 constexpr int kRingStages = 3;              // TMA ring depth when it fits (else two)
