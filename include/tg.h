@@ -105,8 +105,7 @@ typedef struct tg_params {
   int32_t n_bad_word_seqs;
   /* 0/1: renormalize_logits, a log-softmax of the scores after the processors
    * and before temperature.  Selection does not change under it (a per-row
-   * shift); tg_process applies it; tg_beam_step does not take it yet
-   * (TG_ERR_UNSUPPORTED). */
+   * shift); tg_process and tg_beam_step apply it. */
   int32_t renormalize_logits;
 } tg_params;
 

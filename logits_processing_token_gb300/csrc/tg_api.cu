@@ -400,7 +400,7 @@ tg_status tg_beam_step(const void* logits, int32_t num_prompts, int32_t num_beam
                        const int32_t* prompt_lens, const tg_config* cfg, float* out_scores,
                        int32_t* out_tokens, int32_t* out_beams, tg_stream stream) {
   if (!cfg || num_prompts < 0 || num_beams < 1 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
-  if (num_beams > tg::kMaxClusterBeams || cfg->dev.renorm) return TG_ERR_UNSUPPORTED;
+  if (num_beams > tg::kMaxClusterBeams) return TG_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(num_prompts) * num_beams;
   if (rows > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
   if (rows == 0) return TG_OK;

@@ -112,19 +112,29 @@ struct BeamRow {
   const unsigned* N;
   bool bitmaps;
   float lse_hi, lse_lo, bs;
+  // renormalize_logits: the processed log-probabilities less their own
+  // log-sum-exp (r_hi + r_lo); when every token is removed, all score -ln V
+  bool renorm, allf;
+  float r_hi, r_lo, lnv;
 
-  __device__ __forceinline__ float score(float x, int i) const {
+  // processed log-probability -> candidate score
+  __device__ __forceinline__ float fin(float ls) const {
+    if (renorm) ls = allf ? -lnv : clampf(__fsub_rn(__fsub_rn(ls, r_hi), r_lo));
+    return clampf(__fadd_rn(ls, bs));
+  }
+  __device__ __forceinline__ float processed(float x, int i) const {
     float ls = __fsub_rn(__fsub_rn(x, lse_hi), lse_lo);
     if (bitmaps) {
       if (get_bit(N, i)) ls = kFilter;
       else if (get_bit(M, i)) ls = penalize(ls, rho);
     }
-    return clampf(__fadd_rn(ls, bs));
+    return ls;
   }
+  __device__ __forceinline__ float score(float x, int i) const { return fin(processed(x, i)); }
   // An unmarked token's score (no processor changes it).  The bitmaps are not
   // read: N may hold the marked-token list instead of the banned bitmap.
   __device__ __forceinline__ float score_unmarked(float x) const {
-    return clampf(__fadd_rn(__fsub_rn(__fsub_rn(x, lse_hi), lse_lo), bs));
+    return fin(__fsub_rn(__fsub_rn(x, lse_hi), lse_lo));
   }
   // Every token once: 16-byte vectors, four per thread in flight, when the
   // row is 16-byte aligned; the rest element by element.
@@ -246,13 +256,22 @@ __global__ void __launch_bounds__(kThreads, 2) beam_kernel(const DevCfg c, const
     br.bs = a.beam_scores[r];
     br.lse_hi = 0.0f;
     br.lse_lo = 0.0f;
+    br.renorm = c.renorm != 0;
+    br.allf = false;
+    br.r_hi = 0.0f;
+    br.r_lo = 0.0f;
+    br.lnv = logf(static_cast<float>(V));
     if (rm.forced) {
       // every token scores the filter value except the forced ids (0), before
       // the beam's score: the forced ids in index order, then the lowest other ids
       if (tid == 0) {
         int zs[8];
         const int nzall = forced_zeros(c, rm, zs);
-        const float s0 = clampf(__fadd_rn(0.0f, br.bs)), sf = clampf(__fadd_rn(kFilter, br.bs));
+        // renormalized: the forced ids share the mass (-ln nz each), or every
+        // token is removed and all score -ln V
+        br.allf = nzall == 0;
+        br.r_hi = nzall > 0 ? logf(static_cast<float>(nzall)) : 0.0f;
+        const float s0 = br.fin(0.0f), sf = br.fin(kFilter);
         const int nz = s0 > sf ? nzall : 0;   // equal scores: index order alone
         int n = 0;
         for (int q = 0; q < nz && n < kk; ++q) {
@@ -279,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 2) beam_kernel(const DevCfg c, const
       // pass 1: log-sum-exp (each thread keeps (max, sum of exp(x - max)),
       // rescaled when its maximum grows) and the largest unmarked logit
       constexpr int PER = DT == kF32 ? 4 : 8;
-      float tm = -INFINITY, ts = 0.0f, tu = -INFINITY;
+      // (with renormalize_logits also the unmarked tokens' share, tsu)
+      float tm = -INFINITY, ts = 0.0f, tu = -INFINITY, tsu = 0.0f;
       br.pass_vec(
           [&](const float (&x)[PER], int, unsigned mk) {
             float vm = x[0], vu = (mk & 1u) ? -INFINITY : x[0];
@@ -289,21 +309,32 @@ __global__ void __launch_bounds__(kThreads, 2) beam_kernel(const DevCfg c, const
               vu = ((mk >> e) & 1u) ? vu : fmaxf(vu, x[e]);
             }
             if (vm > tm) {
-              ts = tm > -INFINITY ? ts * expf(tm - vm) : 0.0f;
+              const float f = tm > -INFINITY ? expf(tm - vm) : 0.0f;
+              ts *= f;
+              tsu *= f;
               tm = vm;
             }
-            float add = 0.0f;
+            float add = 0.0f, addu = 0.0f;
 #pragma unroll
-            for (int e = 0; e < PER; ++e) add += expf(x[e] - tm);
+            for (int e = 0; e < PER; ++e) {
+              const float ex = expf(x[e] - tm);
+              add += ex;
+              addu += ((mk >> e) & 1u) ? 0.0f : ex;
+            }
             ts += add;
+            tsu += addu;
             tu = fmaxf(tu, vu);
           },
           [&](float x, int, bool mkd) {
             if (x > tm) {
-              ts = tm > -INFINITY ? ts * expf(tm - x) : 0.0f;
+              const float f = tm > -INFINITY ? expf(tm - x) : 0.0f;
+              ts *= f;
+              tsu *= f;
               tm = x;
             }
-            ts += expf(x - tm);
+            const float ex = expf(x - tm);
+            ts += ex;
+            tsu += mkd ? 0.0f : ex;
             if (!mkd) tu = fmaxf(tu, x);
           });
       const float m = block_max(tm, &sm.red);
@@ -325,6 +356,45 @@ __global__ void __launch_bounds__(kThreads, 2) beam_kernel(const DevCfg c, const
       __syncthreads();
       br.lse_hi = sm.lse_hi;
       br.lse_lo = sm.lse_lo;
+      if (br.renorm) {
+        // log-sum-exp of the processed log-probabilities: the unmarked tokens'
+        // share of the row's mass (U / S) plus each marked token's exp(ls)
+        const float U = block_sum_f(tm > -INFINITY ? tsu * expf(tm - m) : 0.0f, &sm.red);
+        float mk = 0.0f;
+        if (nlist >= 0) {
+          for (int j = tid; j < nlist; j += kThreads) {
+            const unsigned ent = N[j];
+            const int t = static_cast<int>(ent & ~kBannedFlag);
+            const float ls = __fsub_rn(__fsub_rn(beam_logit<DT>(row, t), br.lse_hi), br.lse_lo);
+            mk += expf((ent & kBannedFlag) ? kFilter : penalize(ls, br.rho));
+          }
+        } else {
+          br.pass([&](float x, int i) {
+            if (get_bit(M, i)) mk += expf(br.processed(x, i));
+          });
+        }
+        mk = block_sum_f(mk, &sm.red);
+        if (tid == 0) {
+          constexpr double kLn2 = 0.6931471805599453;
+          const double tot = static_cast<double>(U) / static_cast<double>(S) + static_cast<double>(mk);
+          if (!(tot > 0.0)) {
+            sm.lse_hi = 0.0f;
+            sm.lse_lo = -1.0f;   // every token removed
+          } else {
+            const float tf = static_cast<float>(tot);
+            const unsigned b = __float_as_uint(tf);
+            const int e = static_cast<int>(b >> 23) - 127;
+            const float mant = __uint_as_float((b & 0x007fffffu) | 0x3f800000u);
+            const double lse2 = (static_cast<double>(e) + static_cast<double>(log2f(mant))) * kLn2;
+            sm.lse_hi = static_cast<float>(lse2);
+            sm.lse_lo = static_cast<float>(lse2 - static_cast<double>(sm.lse_hi));
+          }
+        }
+        __syncthreads();
+        br.allf = sm.lse_lo == -1.0f && sm.lse_hi == 0.0f;
+        br.r_hi = br.allf ? 0.0f : sm.lse_hi;
+        br.r_lo = br.allf ? 0.0f : sm.lse_lo;
+      }
       TB_T(2);
 
       // Fast path.  An unmarked token's score rises with its logit, so the kk
@@ -431,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2) beam_kernel(const DevCfg c, const
             const float x = beam_logit<DT>(row, t);
             float ls = __fsub_rn(__fsub_rn(x, br.lse_hi), br.lse_lo);
             ls = (ent & kBannedFlag) ? kFilter : penalize(ls, br.rho);
-            const float s = clampf(__fadd_rn(ls, br.bs));
+            const float s = br.fin(ls);
             if (s > sbnd) {
               const int pos = atomicAdd(&sm.ngt, 1);
               if (pos < kMergeCap) { sm.ms[pos] = s; sm.mi[pos] = static_cast<unsigned>(t); }

@@ -2229,8 +2229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sc[i] = s;
   }
   if (c.renorm) {
-    // renormalize_logits: s - logsumexp(s), the log-sum-exp as hi + lo (ln S
-    // from S's exponent and log2f of its mantissa), then temperature
+    // renormalize_logits: (s - m) - ln S with S = sum exp(s - m), ln S as
+    // hi + lo from S's exponent and log2f of its mantissa, then temperature.
+    // The maximum comes off first: a row of equal scores at the filter value
+    // gives -ln V (m + ln S would round back to m there).
     csync();
     float tm = -INFINITY;
     for (int i = threadIdx.x; i < V; i += kThreads) tm = fmaxf(tm, sc[i]);
@@ -2242,10 +2244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned b = __float_as_uint(S);
     const int e = static_cast<int>(b >> 23) - 127;
     const float mant = __uint_as_float((b & 0x007fffffu) | 0x3f800000u);
-    const double lse = static_cast<double>(m) + (static_cast<double>(e) + static_cast<double>(log2f(mant))) * kLn2;
-    const float hi = static_cast<float>(lse), lo = static_cast<float>(lse - static_cast<double>(hi));
+    const double lnS = (static_cast<double>(e) + static_cast<double>(log2f(mant))) * kLn2;
+    const float hi = static_cast<float>(lnS), lo = static_cast<float>(lnS - static_cast<double>(hi));
     for (int i = threadIdx.x; i < V; i += kThreads) {
-      float s = clampf(__fsub_rn(__fsub_rn(sc[i], hi), lo));
+      float s = clampf(__fsub_rn(__fsub_rn(__fsub_rn(sc[i], m), hi), lo));
       if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
       sc[i] = s;
     }

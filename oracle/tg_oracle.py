@@ -414,11 +414,11 @@ def processed_scores(x, h, P, p: Params):
 # ---------------------------------------------------------------------------
 def log_softmax_row(x: np.ndarray) -> np.ndarray:
     """The log-softmax of one row of f32 logits: each x_i - logsumexp(x),
-    with the log-sum-exp in fp64, rounded once to f32."""
-    d = x.astype(np.float64)
-    m = d.max()
-    lse = m + np.log(np.sum(np.exp(d - m)))
-    return (d - lse).astype(np.float32)
+    in fp64, rounded once to f32.  The maximum m comes off first,
+    (x_i - m) - log(sum exp(x - m)), so that a row of equal scores at the
+    filter value (~3.4e38, where m + ln V rounds back to m) still gives -ln V."""
+    d = x.astype(np.float64) - x.astype(np.float64).max()
+    return (d - np.log(np.sum(np.exp(d)))).astype(np.float32)
 
 
 def beam_keep(num_beams: int, p: Params) -> int:

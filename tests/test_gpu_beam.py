@@ -170,3 +170,28 @@ def test_ties_and_all_removed_rows():
     w2 = W.Workload("removed", dict(vocab=V, logits_dtype="f32", suppress_tokens=list(range(V))),
                     logits, ids, off, np.ones(6, np.int32), rng.random(6, dtype=np.float32))
     compare_beam(w2, 3, np.zeros(6, np.float32))
+
+
+@pytest.mark.parametrize("nb", [2, 4])
+def test_renormalize_logits(nb):
+    """Each beam row's processed log-probabilities less their own log-sum-exp,
+    then the beam's score; forced rows share their mass, an all-removed row
+    scores -ln V everywhere."""
+    w = W.random_case(81 + nb, B=3 * nb, V=1000, dtype="f32", mode="greedy", L_max=40, repetition_penalty=1.6,
+                      no_repeat_ngram_size=2, suppress_tokens=list(range(40)), renormalize_logits=True)
+    bs = np.random.default_rng(nb).normal(-3, 1, w.B).astype(np.float32)
+    compare_beam(w, nb, bs)
+    V = 3000
+    rng = np.random.default_rng(8)
+    hists = [[1, 2, 3, 4, 5], [7], [4, 5, 6], [11], [9, 9, 9], [5, 6, 7, 8]]
+    plens = [2, 1, 1, 1, 2, 1]
+    ids, off = W._pack([np.array(h, np.int32) for h in hists])
+    logits = rng.normal(0, 2, (6, V)).astype(np.float32)
+    params = dict(vocab=V, logits_dtype="f32", mode="greedy", eos_token_ids=[2], forced_eos_token_ids=[2, 5],
+                  max_new_tokens=4, forced_bos_token_id=7, suppress_tokens=[5], repetition_penalty=1.2,
+                  renormalize_logits=True)
+    w2 = W.Workload("forced", params, logits, ids, off, np.array(plens, np.int32), rng.random(6, dtype=np.float32))
+    compare_beam(w2, 3, np.array([-1.0, -2.0, -3.0, -0.5, -9.0, -2.5], np.float32))
+    w3 = W.Workload("removed", dict(vocab=V, logits_dtype="f32", suppress_tokens=list(range(V)), renormalize_logits=True),
+                    logits, ids, off, np.ones(6, np.int32), rng.random(6, dtype=np.float32))
+    compare_beam(w3, 2, np.zeros(6, np.float32))

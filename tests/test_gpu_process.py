@@ -113,17 +113,24 @@ def test_process_renormalize_logits(mode):
         assert np.array_equal(sc[b][banned], s_ref[banned])
 
 
-def test_beam_step_rejects_renormalize():
-    import torch
-    import logits_processing_token_gb300 as tg
-    cfg = tg.Config(vocab=64, renormalize_logits=True)
-    x = torch.zeros((2, 64), device="cuda")
-    z = torch.zeros(2, device="cuda")
-    off = torch.tensor([0, 1, 2], dtype=torch.int64, device="cuda")
-    ids = torch.tensor([1, 2], dtype=torch.int32, device="cuda")
-    pl = torch.ones(2, dtype=torch.int32, device="cuda")
-    keep = tg.tg_beam_keep(cfg, 2)
-    s = torch.zeros((1, keep), device="cuda")
-    t = torch.zeros((1, keep), dtype=torch.int32, device="cuda")
-    with pytest.raises(tg.TGError):
-        tg.tg_beam_step(x, z, ids, off, pl, cfg, 2, s, t, t.clone())
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_process_renormalize_degenerate_rows(mode):
+    """renormalize_logits on a row with every token removed (-ln V everywhere,
+    before temperature) and on rows forced to one token (0 there)."""
+    V = 3000
+    rng = np.random.default_rng(71)
+    logits = rng.normal(0, 2, (3, V)).astype(np.float32)
+    ids, off = W._pack([np.array(h, np.int32) for h in ([1, 2, 3], [4], [5, 6])])
+    uni = rng.random(3, dtype=np.float32)
+    for params in (dict(suppress_tokens=list(range(V))),
+                   dict(forced_bos_token_id=7, forced_eos_token_ids=[9], max_new_tokens=1)):
+        w = W.Workload("degenerate", dict(vocab=V, logits_dtype="f32", mode=mode, temperature=0.5,
+                                          renormalize_logits=True, **params),
+                       logits, ids, off, np.array([1, 1, 1], np.int32), uni)
+        sc, _, _ = run_process(w)
+        p = O.Params(**w.params)
+        for b in range(3):
+            x = O.upcast_row(w.logits[b], p.logits_dtype)
+            s_ref, _ = O.processed_scores(x, list(w.history(b)), 1, p)
+            d = np.abs(sc[b].astype(np.float64) - s_ref.astype(np.float64))
+            assert np.all(d <= 2e-6 * np.maximum(1.0, np.abs(s_ref.astype(np.float64)))), (b, d.max())

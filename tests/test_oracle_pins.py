@@ -680,3 +680,19 @@ def test_renormalize_logits_is_a_normalised_shift():
             a = O.select_row(x, [1, 2, 5], 1, P(vocab=V, mode=mode, renormalize_logits=True, top_p=0.8), u)
             b = O.select_row(x, [1, 2, 5], 1, P(vocab=V, mode=mode, top_p=0.8), u)
             assert a[0] == b[0]
+
+
+def test_renormalize_logits_degenerate_rows():
+    """Equal scores give the uniform distribution, log 1/V, at any level:
+    the filter value included (every token removed); one kept token gets
+    log 1 = 0 and the rest stay removed."""
+    V = 3000
+    for level in (0.0, -7.5, 1e30, F):
+        assert (O.log_softmax_row(np.full(V, level, np.float32)) == np.float32(-math.log(V))).all(), level
+    x = np.random.default_rng(62).normal(0, 2, V).astype(np.float32)
+    s, banned = O.processed_scores(x, [1, 2], 1, P(vocab=V, suppress_tokens=list(range(V)), renormalize_logits=True))
+    assert banned.all() and (s == np.float32(-math.log(V))).all()
+    # length 1 = max_length - 1 (prompt 1, one new token): eos 9 forced
+    s, banned = O.processed_scores(x, [1], 1, P(vocab=V, max_new_tokens=1, forced_eos_token_ids=[9],
+                                                    renormalize_logits=True))
+    assert s[9] == 0.0 and (s[np.arange(V) != 9] == F).all()
