@@ -250,3 +250,39 @@ def beam_workload(prompts: int = 64, beams: int = 4, V: int = 151_936, seed: int
     w.extra["beam_scores"] = bs
     w.extra["beams"] = beams
     return w
+
+
+def processor_state(seed: int, rows: int, V: int, processors, fill: float = 0.6, hot=None,
+                    set_removed: float = 0.3, sigma: float = 3.0):
+    """A state for the task's processors, one row per logits row: for each
+    (kind, size) processor, about fill * size distinct ids per row in
+    ascending order followed by -1 padding, half of them (when ``hot`` gives
+    each row's preferred ids) drawn from hot[r], the rest uniform over
+    [0, V).  Values are N(0, sigma^2); a "set" entry is the filter value
+    (-FLT_MAX, a removal) with probability ``set_removed``.  Returns
+    (ids int32 [rows, S], values f32 [rows, S])."""
+    rng = np.random.default_rng(seed)
+    S = sum(int(n) for _, n in processors)
+    ids = np.full((rows, S), -1, np.int32)
+    vals = np.zeros((rows, S), np.float32)
+    neg_max = -np.finfo(np.float32).max
+    for r in range(rows):
+        col = 0
+        for kind, size in processors:
+            size = int(size)
+            m = min(int(rng.binomial(size, fill)), V)
+            pool = set()
+            if hot is not None and len(hot[r]):
+                hr = np.asarray(hot[r])
+                take = rng.choice(hr.size, size=min(hr.size, m // 2 + 1), replace=False)
+                pool.update(int(hr[q]) for q in take)
+            while len(pool) < m:
+                pool.add(int(rng.integers(0, V)))
+            chosen = sorted(int(t) for t in rng.permutation(sorted(pool))[:m])
+            ids[r, col:col + len(chosen)] = chosen
+            v = (rng.standard_normal(len(chosen)) * sigma).astype(np.float32)
+            if kind in ("set", 1):
+                v[rng.random(len(chosen)) < set_removed] = neg_max
+            vals[r, col:col + len(chosen)] = v
+            col += size
+    return ids, vals

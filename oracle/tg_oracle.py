@@ -11,8 +11,12 @@ What it computes, step by step, in the order the pages give:
   selection: the processors run in the order repetition_penalty,
   no_repeat_ngram_size, single-token bad_words_ids, min_length /
   min_new_tokens, forced_bos_token_id, forced_eos_token_id, suppress_tokens,
-  begin_suppress_tokens, (task processors, renormalize_logits: not built),
+  begin_suppress_tokens, the task's processors, renormalize_logits,
   temperature, top_k, top_p.
+* Same page, section "Processors": a processor is a per-row state made on the
+  host before each step plus a function of the row's scores and that state;
+  the task's come at the end of the list.  Here the functions are "bias"
+  (s + v) and "set" (v) over a sparse state of (id, value) entries.
 * Same page, section "Lengths": a row's length L counts the prompt and the new
   tokens; max_length = prompt + max_new_tokens; the rules for
   no_repeat_ngram_size, min_length, min_new_tokens, forced_bos, forced_eos and
@@ -87,6 +91,9 @@ class Params:
     top_k: int = 0
     top_p: float = 1.0
     renormalize_logits: bool = False   # log-softmax after the processors (diagnostic scores, beam step)
+    # the task's processors: (kind, size) pairs, kind "bias" (s + v) or "set" (v); each owns
+    # `size` columns of the per-row state (ids, values) passed next to the logits
+    processors: Sequence[tuple] = ()
 
 
 @dataclass
@@ -99,6 +106,7 @@ class RowInfo:
     n_kept: int = 0                  # tokens kept for the draw
     forced: bool = False
     logprob: float = float("nan")    # log-softmax of the selected-from scores at the token
+    bad_state: bool = False          # the processors' state broke its layout and was dropped
 
 
 # ---------------------------------------------------------------------------
@@ -184,11 +192,52 @@ def ngram_banned_tokens(h: Sequence[int], n: int) -> list[int]:
 # ---------------------------------------------------------------------------
 # a0-a9: the processors, in order
 # ---------------------------------------------------------------------------
-def process_row(x: np.ndarray, h: Sequence[int], P: int, p: Params):
-    """Scores after a0-a9 for one non-empty row.
+def processor_state_valid(ids_row, p: Params) -> bool:
+    """A row's processors' state keeps its layout: every id is -1 or in
+    [0, V); within a processor's columns the used ids ascend strictly and the
+    unused (-1) come after them."""
+    col = 0
+    for _, size in p.processors:
+        block = [int(t) for t in ids_row[col:col + size]]
+        col += size
+        used = [t for t in block if t != -1]
+        if any(t < -1 or t >= p.vocab for t in block):
+            return False
+        if block[:len(used)] != used or any(b <= a for a, b in zip(used, used[1:])):
+            return False
+    return True
+
+
+def apply_processors(s: np.ndarray, state, p: Params, info) -> None:
+    """The task's processors (Transmuter.Generation, section "Processors"),
+    in list order, on the scores after a9: processor k reads its columns of
+    the row's state; an entry (t, v) makes s[t] = s[t] + v ("bias", an f32
+    add) or v ("set"), never below the filter value.  A state that breaks
+    its layout is dropped (info.bad_state)."""
+    ids_row, vals_row = state
+    if not processor_state_valid(ids_row, p):
+        info.bad_state = True
+        return
+    col = 0
+    for kind, size in p.processors:
+        bias = kind in ("bias", 0)
+        for j in range(col, col + size):
+            t = int(ids_row[j])
+            if t < 0:
+                continue
+            v = F32(vals_row[j])
+            with np.errstate(over="ignore"):
+                new = F32(s[t] + v) if bias else v
+            s[t] = max(new, FILTER)
+        col += size
+
+
+def process_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, state=None):
+    """Scores after a0-a9 and the task's processors for one non-empty row
+    (state: the row's (ids, values), needed when p has processors).
 
     Returns (s, banned, info): s are fp32 scores, banned marks tokens a
-    ban/force processor set to the filter value.
+    ban/force processor of a3-a9 set to the filter value.
     """
     V = p.vocab
     L = len(h)
@@ -252,6 +301,9 @@ def process_row(x: np.ndarray, h: Sequence[int], P: int, p: Params):
         for t in p.begin_suppress_tokens:
             s[t] = FILTER
             banned[t] = True
+    # the task's processors, at the end of the list
+    if p.processors:
+        apply_processors(s, state, p, info)
     return s, banned, info
 
 
@@ -357,7 +409,7 @@ def selected_from_scores(s_t: np.ndarray, order: np.ndarray, n_kept: int, s_k: n
     return out
 
 
-def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float):
+def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float, state=None):
     """One row of tg_select.  Returns (token id or -1, RowInfo); the info
     carries the token's log-probability (NaN for a padding row).
 
@@ -366,7 +418,7 @@ def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float):
     under it (exactly, before rounding), so selection leaves it out."""
     if len(h) == 0:
         return -1, RowInfo()
-    s, _, info = process_row(x, h, P, p)
+    s, _, info = process_row(x, h, P, p, state)
     if p.mode == "greedy":
         tok = int(np.argmax(s))
         info.logprob = log_softmax_at(s, tok)
@@ -381,9 +433,14 @@ def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float):
     return tok, info
 
 
+def _row_state(proc_state, r):
+    return None if proc_state is None else (proc_state[0][r], proc_state[1][r])
+
+
 def select(logits, hist_ids, hist_offsets, prompt_lens, p: Params, uniforms=None,
-           rows=None):
-    """tg_select over a batch (or the listed ``rows``) -> (ids, infos)."""
+           rows=None, proc_state=None):
+    """tg_select over a batch (or the listed ``rows``) -> (ids, infos).
+    proc_state: (ids [B, S], values [B, S]) of the task's processors."""
     B = len(prompt_lens)
     rows = range(B) if rows is None else rows
     ids, infos = [], []
@@ -391,16 +448,16 @@ def select(logits, hist_ids, hist_offsets, prompt_lens, p: Params, uniforms=None
         h = hist_ids[int(hist_offsets[b]):int(hist_offsets[b + 1])]
         x = upcast_row(logits[b], p.logits_dtype)
         u = float(uniforms[b]) if uniforms is not None else 0.0
-        t, info = select_row(x, h, int(prompt_lens[b]), p, u)
+        t, info = select_row(x, h, int(prompt_lens[b]), p, u, _row_state(proc_state, b))
         ids.append(t)
         infos.append(info)
     return np.array(ids, dtype=np.int32), infos
 
 
-def processed_scores(x, h, P, p: Params):
+def processed_scores(x, h, P, p: Params, state=None):
     """What the diagnostic entry point writes: scores after a0-a9 (greedy) or
     a0-a10 (sampling), and the mask of banned tokens."""
-    s, banned, _ = process_row(x, h, P, p)
+    s, banned, _ = process_row(x, h, P, p, state)
     if p.renormalize_logits:
         s = _clamp(log_softmax_row(s))
     if p.mode == "sample":
@@ -426,7 +483,8 @@ def beam_keep(num_beams: int, p: Params) -> int:
     return max(2, 1 + len(p.eos_token_ids)) * num_beams
 
 
-def beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams: int, p: Params):
+def beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams: int, p: Params,
+              proc_state=None):
     """One beam-search step on the device side.
 
     Rows i*num_beams .. i*num_beams+num_beams-1 are prompt i's beams.  Each
@@ -444,7 +502,8 @@ def beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beam
     out_t = np.zeros((P, K), np.int32)
     out_b = np.zeros((P, K), np.int32)
     for i in range(P):
-        cand, live = beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams, p, i)
+        cand, live = beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams, p, i,
+                                     proc_state)
         flat = order_desc(cand)
         flat = flat[live[flat]][:K]
         n = flat.size
@@ -458,7 +517,8 @@ def beam_step(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beam
     return out_s, out_t, out_b
 
 
-def beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams: int, p: Params, i: int):
+def beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, num_beams: int, p: Params, i: int,
+                    proc_state=None):
     """Prompt i's num_beams * V candidate scores (flat index b*V + t) and a
     mask of the live ones (rows with an empty history give none)."""
     V = p.vocab
@@ -471,7 +531,7 @@ def beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, nu
             continue
         x = upcast_row(logits[r], p.logits_dtype)
         ls = log_softmax_row(x)
-        s, _, _ = process_row(ls, h, int(prompt_lens[r]), p)
+        s, _, _ = process_row(ls, h, int(prompt_lens[r]), p, _row_state(proc_state, r))
         if p.renormalize_logits:
             s = _clamp(log_softmax_row(s))
         with np.errstate(over="ignore"):

@@ -696,3 +696,108 @@ def test_renormalize_logits_degenerate_rows():
     s, banned = O.processed_scores(x, [1], 1, P(vocab=V, max_new_tokens=1, forced_eos_token_ids=[9],
                                                     renormalize_logits=True))
     assert s[9] == 0.0 and (s[np.arange(V) != 9] == F).all()
+
+
+# --------------------------------------------------------------------------
+# The task's processors (Transmuter.Generation, section "Processors"): at the
+# end of the list, after begin_suppress_tokens, before renormalize_logits and
+# temperature; here "bias" (s + v) and "set" (v) over a sparse per-row state
+# --------------------------------------------------------------------------
+def _state(*blocks):
+    """One row's state from per-processor lists of (id, value), padded to the block sizes given."""
+    ids, vals = [], []
+    for entries, size in blocks:
+        for t, v in entries:
+            ids.append(t)
+            vals.append(v)
+        ids += [-1] * (size - len(entries))
+        vals += [0.0] * (size - len(entries))
+    return np.array(ids, np.int32), np.array(vals, np.float32)
+
+
+def test_processor_bias_after_the_penalty_and_only_on_listed_ids():
+    V = 6
+    x = np.array([2.0, -1.0, 0.5, 0.25, 3.0, -2.0], np.float32)
+    p = P(vocab=V, repetition_penalty=2.0, processors=(("bias", 3),))
+    st = _state(([(0, 0.25), (2, 0.5), (5, -1.0)], 3))
+    s, banned, info = O.process_row(x, [0, 1], 1, p, st)
+    # history ids 0, 1 penalised first (2 / 2 = 1, -1 * 2 = -2), then the bias;
+    # token 2 is listed but not in the history: no penalty
+    assert s.tolist() == [1.25, -2.0, 1.0, 0.25, 3.0, -3.0]
+    assert not banned.any() and not info.bad_state
+
+
+def test_processors_apply_in_list_order():
+    V = 4
+    x = np.zeros(V, np.float32)
+    a = _state(([(1, 1.0)], 1), ([(1, 5.0)], 1))
+    s, _, _ = O.process_row(x, [0], 1, P(vocab=V, processors=(("bias", 1), ("set", 1))), a)
+    assert s[1] == 5.0
+    s, _, _ = O.process_row(x, [0], 1, P(vocab=V, processors=(("set", 1), ("bias", 1))), a)
+    assert s[1] == 6.0
+
+
+def test_processor_set_to_filter_equals_suppress_and_set_after_suppress_restores():
+    rng = np.random.default_rng(63)
+    V = 50
+    x = rng.normal(0, 2, V).astype(np.float32)
+    h = [3, 4, 4, 9]
+    removed = [5, 11, 30]
+    st = _state(([(t, float(F)) for t in removed], 4))
+    s1, _, _ = O.process_row(x, h, 2, P(vocab=V, repetition_penalty=1.3, processors=(("set", 4),)), st)
+    s2, _, _ = O.process_row(x, h, 2, P(vocab=V, repetition_penalty=1.3, suppress_tokens=removed))
+    assert np.array_equal(s1, s2)
+    # the task's processors run after suppress_tokens: a set brings a token back
+    s3, banned, _ = O.process_row(x, h, 2, P(vocab=V, suppress_tokens=[7], processors=(("set", 1),)),
+                                  _state(([(7, 1.5)], 1)))
+    assert s3[7] == np.float32(1.5) and banned[7]
+
+
+def test_forced_row_bias_gives_the_closed_form_distribution():
+    """Forced eos ids 2 and 5 both score 0; a bias of ln 3 on 5 makes the draw
+    pick 5 with probability 3/4 (it comes first, higher score) and 2 with 1/4."""
+    V = 20
+    x = np.random.default_rng(64).normal(0, 1, V).astype(np.float32)
+    st = _state(([(5, float(np.float32(math.log(3.0))))], 2))
+    kw = dict(vocab=V, max_new_tokens=2, forced_eos_token_ids=[2, 5], processors=(("bias", 2),))
+    h = [1, 9]          # prompt 1 + one new token: L = P + max_new - 1
+    tok, info = O.select_row(x, h, 1, P(mode="greedy", **kw), 0.0, st)
+    assert tok == 5 and info.logprob == pytest.approx(math.log(0.75), abs=1e-6)
+    for u, want in ((0.0, 5), (0.74, 5), (0.76, 2), (0.999, 2)):
+        tok, info = O.select_row(x, h, 1, P(mode="sample", **kw), u, st)
+        assert tok == want, (u, tok)
+        assert info.logprob == pytest.approx(math.log(0.75 if want == 5 else 0.25), abs=1e-6)
+
+
+def test_temperature_after_the_processors():
+    V = 8
+    x = np.zeros(V, np.float32)
+    s, _ = O.processed_scores(x, [1], 1, P(vocab=V, mode="sample", temperature=0.5, processors=(("set", 1),)),
+                              _state(([(3, 3.0)], 1)))
+    assert s[3] == 6.0 and s[0] == 0.0
+
+
+def test_beam_candidates_with_a_bias_and_renormalize():
+    """Equal logits: every log-probability is -ln 4; a bias of ln 3 on token 1
+    and renormalize give log 3/6 there and log 1/6 elsewhere, plus the beam score."""
+    V = 4
+    logits = np.zeros((1, V), np.float32)
+    ids, off = np.array([0], np.int32), np.array([0, 1], np.int64)
+    st = _state(([(1, float(np.float32(math.log(3.0))))], 1))
+    p = P(vocab=V, renormalize_logits=True, processors=(("bias", 1),))
+    cand, live = O.beam_candidates(logits, np.array([-2.0], np.float32), ids, off, np.array([1], np.int32), 1, p, 0,
+                                   (st[0][None, :], st[1][None, :]))
+    want = np.array([math.log(1 / 6), math.log(3 / 6), math.log(1 / 6), math.log(1 / 6)]) - 2.0
+    assert live.all() and np.allclose(cand, want, atol=1e-6)
+
+
+def test_invalid_processor_state_is_dropped():
+    V = 10
+    x = np.arange(V, dtype=np.float32)
+    p = P(vocab=V, processors=(("bias", 3),))
+    for ids in ([4, 2, -1], [1, -1, 3], [2, 2, -1], [0, 10, -1], [-2, -1, -1]):
+        st = (np.array(ids, np.int32), np.ones(3, np.float32))
+        assert not O.processor_state_valid(st[0], p)
+        s, _, info = O.process_row(x, [1], 1, p, st)
+        assert info.bad_state and np.array_equal(s, x)
+    assert O.processor_state_valid(np.array([0, 9, -1], np.int32), p)
