@@ -40,6 +40,9 @@ def parse_args():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--beam", action="store_true",
                     help="time tg_beam_step (64 prompts x 4 beams over the same rows) instead of tg_select")
+    ap.add_argument("--state", action="store_true",
+                    help="time tg_select_state (the benchmark rows with a bias of 64 and a set of 32 state columns "
+                         "per row) instead of tg_select")
     ap.add_argument("--logprobs", action="store_true",
                     help="time tg_select_logprobs (ids plus each token's log-probability) instead of tg_select")
     return ap.parse_args()
@@ -413,12 +416,76 @@ def run_beam(args):
     print(json.dumps(line), flush=True)
 
 
+def run_state(args):
+    """tg_select_state over the benchmark rows with the task's processors: a
+    bias of 64 and a set of 32 state columns per row (half of a row's ids from
+    its history)."""
+    import numpy as np
+    import torch
+    from logits_processing_token_gb300 import _build
+    _build.build()
+    import logits_processing_token_gb300 as tg
+    from logits_processing_token_gb300 import workloads as W
+
+    procs = (("bias", 64), ("set", 32))
+    w = W.config3()
+    w.params["processors"] = procs
+    hot = [np.asarray(w.history(b)) for b in range(w.B)]
+    st_ids, st_vals = W.processor_state(5, w.B, w.V, procs, hot=hot)
+    cfg = tg.Config(**w.params)
+    row_bytes = w.B * w.V * 2
+    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / row_bytes)))
+    host_logits = torch.from_numpy(w.logits.view(np.int16))
+    sets = [host_logits.cuda().view(torch.bfloat16) for _ in range(n_sets)]
+    hid = torch.from_numpy(w.hist_ids).cuda()
+    off = torch.from_numpy(w.hist_offsets).cuda()
+    pl = torch.from_numpy(w.prompt_lens).cuda()
+    u = torch.from_numpy(w.uniforms).cuda()
+    sid = torch.from_numpy(st_ids).cuda()
+    sval = torch.from_numpy(st_vals).cuda()
+    out = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    lp = torch.empty(w.B, dtype=torch.float32, device="cuda") if args.logprobs else None
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        tg.tg_select_state(sets[i % n_sets], hid, off, pl, cfg, sid, sval, u, out, out_logprobs=lp, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    peak, peak_kind = measured_peak()
+    alg, _ = required_bytes(w)
+    alg += int(st_ids.size) * 8
+    achieved = alg / (ms / 1000.0) / 1e9
+    line = {"metric": "rows/s with the task's processors (tg_select_state)", "value": w.B / (ms / 1000.0),
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD + "; processors bias 64 + set 32 state columns per row",
+                       "logprobs": bool(args.logprobs),
+                       "l2": "inputs rotate over %d copies of the logits > L2" % n_sets},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": "%s hbm_gbs (copy)" % peak_kind,
+                         "bytes_per_launch": alg, "kernel": "state_kernel<bf16>", "traffic": None},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.beam:
         run_beam(args)
+    elif args.state:
+        run_state(args)
     else:
         run_ours(args)
 

@@ -59,12 +59,23 @@ typedef enum { TG_GREEDY = 0, TG_SAMPLE = 1 } tg_mode;
 #define TG_FLAG_HISTORY_ID_OUT_OF_RANGE 0x1u /* a history id was < 0 or >= V; skipped */
 #define TG_FLAG_BAD_ROW 0x2u                 /* offsets/prompt length inconsistent; row gave -1 */
 #define TG_FLAG_SLOW_PATH 0x4u               /* a row needed the multi-pass exact path */
+#define TG_FLAG_BAD_STATE 0x10u              /* a row's processor state broke its layout; dropped */
 
 /* Largest vocabulary the kernels take. */
 #define TG_MAX_VOCAB (1 << 18)
 /* Longest list accepted for eos ids and forced eos ids. */
 #define TG_MAX_BAD_WORD_LEN 16
 #define TG_MAX_EOS 8
+/* The task's processors: at most this many, owning at most this many state
+ * columns in all. */
+#define TG_MAX_PROCESSORS 8
+#define TG_MAX_STATE_COLS 4096
+
+/* Kinds of the task's processors (tg_params.processor_kinds). */
+typedef enum {
+  TG_PROC_BIAS = 0, /* s + v for each (id, v) of the row's state */
+  TG_PROC_SET = 1   /* v for each (id, v) of the row's state */
+} tg_proc_kind;
 
 /*
  * Generation settings, named after transformers' generation_config fields.
@@ -107,6 +118,17 @@ typedef struct tg_params {
    * and before temperature.  Selection does not change under it (a per-row
    * shift); tg_process and tg_beam_step apply it. */
   int32_t renormalize_logits;
+  /* The task's processors (Transmuter.Generation, section "Processors": a
+   * per-row state made before the step, and a function of the row's scores
+   * and that state; they run after begin_suppress_tokens and before
+   * renormalize_logits and temperature, in list order).  Processor k has
+   * kind processor_kinds[k] (tg_proc_kind) and owns processor_sizes[k] >= 1
+   * consecutive columns of the state; S = the sum of the sizes.  A config
+   * with processors is used through tg_select_state and tg_process_state
+   * only; the other entry points that take a config refuse it. */
+  const int32_t* processor_kinds;
+  const int32_t* processor_sizes;
+  int32_t n_processors; /* 0 .. TG_MAX_PROCESSORS; S <= TG_MAX_STATE_COLS */
 } tg_params;
 
 /* Opaque, immutable after creation; holds the constant masks on the device. */
@@ -265,6 +287,45 @@ tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, con
                             const int32_t* hist_ids, const int64_t* hist_offsets, const int32_t* prompt_lens,
                             const tg_config* cfg, const float* uniforms, int32_t* out_match, int32_t* out_next,
                             tg_stream stream);
+
+/*
+ * tg_select_state -- tg_select (or tg_select_logprobs) with the task's
+ * processors of cfg (Transmuter.Generation, section "Processors").
+ *
+ *  state_ids     device int32 [B, S]: row b's state is state_ids[b*S ..
+ *                b*S + S); processor k reads its own columns.  Within a
+ *                processor's columns the ids in use come first, strictly
+ *                ascending, each in [0, V), and the unused columns hold -1.
+ *  state_values  device f32 [B, S]: the value of each (id) entry.  A "bias"
+ *                entry (t, v) makes s[t] + v (an f32 add), a "set" entry
+ *                makes v; either never goes below the filter value.
+ *  out_logprobs  device f32 [B] or NULL: as tg_select_logprobs.
+ *
+ * The processors run on the scores after the processors of tg_select (also
+ * on a forced row, whose other tokens hold the filter value) and before
+ * temperature, top_k, top_p and the draw.  A row whose state breaks its
+ * layout runs without the processors and raises TG_FLAG_BAD_STATE.  One
+ * thread block per row reads the row from global memory in several passes
+ * (the multi-pass exact selection of tg_select); it does not count rows as
+ * slow.  Other arguments, layouts and errors as tg_select; a cfg without
+ * processors, or a NULL state pointer, is TG_ERR_INVALID_ARGUMENT.
+ */
+tg_status tg_select_state(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                          const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                          const int32_t* state_ids, const float* state_values, const float* uniforms,
+                          int32_t* out_ids, float* out_logprobs, tg_stream stream);
+
+/*
+ * tg_process_state -- tg_process with the task's processors: the scores
+ * tg_select_state selects from (diagnostic, not tuned).  state_ids and
+ * state_values as tg_select_state; out_banbits marks what the processors of
+ * tg_select set to the filter value (the task's processors do not change
+ * it).  Other arguments as tg_process.
+ */
+tg_status tg_process_state(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                           const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                           const int32_t* state_ids, const float* state_values, float* out_scores,
+                           uint32_t* out_banbits, float* out_probs, tg_stream stream);
 
 /* Read (synchronously) the sticky status bits and the count of rows that took
  * the multi-pass exact path since the last clear. */

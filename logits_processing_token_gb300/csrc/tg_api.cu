@@ -27,6 +27,7 @@ struct tg_config {
   int nwords = 0;
   LaunchPlan sel, ver;
   int proc_smem = 0;
+  int state_smem = 0;
   void* dmem = nullptr;
 };
 
@@ -125,6 +126,17 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   if (p->top_k < 0) return TG_ERR_INVALID_ARGUMENT;
   if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return TG_ERR_INVALID_ARGUMENT;
   if (p->max_batch < 0) return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_processors < 0 || p->n_processors > TG_MAX_PROCESSORS) return TG_ERR_INVALID_ARGUMENT;
+  if (p->n_processors > 0) {
+    if (!p->processor_kinds || !p->processor_sizes) return TG_ERR_INVALID_ARGUMENT;
+    long long cols = 0;
+    for (int32_t k = 0; k < p->n_processors; ++k) {
+      if (p->processor_kinds[k] != TG_PROC_BIAS && p->processor_kinds[k] != TG_PROC_SET) return TG_ERR_INVALID_ARGUMENT;
+      if (p->processor_sizes[k] < 1) return TG_ERR_INVALID_ARGUMENT;
+      cols += p->processor_sizes[k];
+    }
+    if (cols > TG_MAX_STATE_COLS) return TG_ERR_INVALID_ARGUMENT;
+  }
   if (p->n_bad_word_seqs < 0) return TG_ERR_INVALID_ARGUMENT;
   if (p->n_bad_word_seqs > 0) {
     if (!p->bad_word_seq_offsets || p->bad_word_seq_offsets[0] != 0) return TG_ERR_INVALID_ARGUMENT;
@@ -207,6 +219,12 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   c.temp = p->temperature;
   c.top_k = p->top_k;
   c.top_p = p->top_p;
+  c.nproc = p->n_processors;
+  c.pcol[0] = 0;
+  for (int k = 0; k < c.nproc; ++k) {
+    c.pkind[k] = p->processor_kinds[k];
+    c.pcol[k + 1] = c.pcol[k] + p->processor_sizes[k];
+  }
   c.tickets = reinterpret_cast<unsigned*>(d + o_tick);
   c.status = reinterpret_cast<unsigned*>(d + o_status);
   c.slow_rows = reinterpret_cast<unsigned long long*>(d + o_slow);
@@ -214,6 +232,7 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   st = plan_select(c.dtype, false, cfg->nwords, &cfg->sel);
   if (st == TG_OK) st = plan_select(c.dtype, true, 0, &cfg->ver);
   cfg->proc_smem = tg::process_smem_bytes(cfg->nwords);
+  cfg->state_smem = tg::state_smem_bytes(cfg->nwords);
   if (st != TG_OK) {
     cudaFree(cfg->dmem);
     delete cfg;
@@ -235,7 +254,7 @@ namespace {
 tg_status select_impl(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
                       const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
                       const float* uniforms, int32_t* out_ids, float* out_logprobs, tg_stream stream) {
-  if (!cfg || B < 0 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
+  if (!cfg || B < 0 || V != cfg->V || cfg->dev.nproc > 0) return TG_ERR_INVALID_ARGUMENT;
   if (B == 0) return TG_OK;
   if (!logits || !hist_offsets || !prompt_lens || !out_ids) return TG_ERR_INVALID_ARGUMENT;
   if (cfg->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
@@ -286,7 +305,7 @@ tg_status tg_select_logprobs(const void* logits, int32_t B, int32_t V, const int
 tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids, int32_t K,
                     const tg_config* cfg, const float* uniforms, int32_t* out_match, int32_t* out_next,
                     tg_stream stream) {
-  if (!cfg || B < 0 || V != cfg->V || K < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (!cfg || B < 0 || V != cfg->V || K < 1 || cfg->dev.nproc > 0) return TG_ERR_INVALID_ARGUMENT;
   if (B == 0) return TG_OK;
   if (B > cfg->max_batch) return TG_ERR_INVALID_ARGUMENT;
   if (!target_logits || !cand_ids || !out_match || !out_next) return TG_ERR_INVALID_ARGUMENT;
@@ -314,7 +333,7 @@ tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, con
                             const int32_t* hist_ids, const int64_t* hist_offsets, const int32_t* prompt_lens,
                             const tg_config* cfg, const float* uniforms, int32_t* out_match, int32_t* out_next,
                             tg_stream stream) {
-  if (!cfg || B < 0 || V != cfg->V || K < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (!cfg || B < 0 || V != cfg->V || K < 1 || cfg->dev.nproc > 0) return TG_ERR_INVALID_ARGUMENT;
   if (B == 0) return TG_OK;
   if (B > cfg->max_batch) return TG_ERR_INVALID_ARGUMENT;
   if (!target_logits || !cand_ids || !out_match || !out_next || !hist_offsets || !prompt_lens)
@@ -344,12 +363,16 @@ tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, con
   return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
-                     const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
-                     float* out_scores, uint32_t* out_banbits, float* out_probs, tg_stream stream) {
+namespace {
+tg_status process_impl(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                       const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                       const int32_t* state_ids, const float* state_values, float* out_scores,
+                       uint32_t* out_banbits, float* out_probs, tg_stream stream) {
   if (!cfg || B < 0 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
+  if ((cfg->dev.nproc > 0) != (state_ids != nullptr)) return TG_ERR_INVALID_ARGUMENT;
   if (B == 0) return TG_OK;
   if (!logits || !hist_offsets || !prompt_lens || !out_scores) return TG_ERR_INVALID_ARGUMENT;
+  if (state_ids && !state_values) return TG_ERR_INVALID_ARGUMENT;
   tg_status st = check_device(cfg);
   if (st != TG_OK) return st;
   tg::SelArgs a{};
@@ -362,7 +385,62 @@ tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hi
   a.plen = prompt_lens;
   a.nwords = cfg->nwords;
   return from_cuda(tg::launch_process(cfg->dev, a, out_scores, out_banbits, out_probs, cfg->proc_smem,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+                                      reinterpret_cast<cudaStream_t>(stream), state_ids, state_values));
+}
+}  // namespace
+
+tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                     const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                     float* out_scores, uint32_t* out_banbits, float* out_probs, tg_stream stream) {
+  return process_impl(logits, B, V, hist_ids, hist_offsets, prompt_lens, cfg, nullptr, nullptr, out_scores,
+                      out_banbits, out_probs, stream);
+}
+
+tg_status tg_process_state(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                           const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                           const int32_t* state_ids, const float* state_values, float* out_scores,
+                           uint32_t* out_banbits, float* out_probs, tg_stream stream) {
+  if (!state_ids || !state_values) return TG_ERR_INVALID_ARGUMENT;
+  return process_impl(logits, B, V, hist_ids, hist_offsets, prompt_lens, cfg, state_ids, state_values, out_scores,
+                      out_banbits, out_probs, stream);
+}
+
+tg_status tg_select_state(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
+                          const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
+                          const int32_t* state_ids, const float* state_values, const float* uniforms,
+                          int32_t* out_ids, float* out_logprobs, tg_stream stream) {
+  if (!cfg || B < 0 || V != cfg->V || cfg->dev.nproc < 1) return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (!logits || !hist_offsets || !prompt_lens || !out_ids || !state_ids || !state_values)
+    return TG_ERR_INVALID_ARGUMENT;
+  if (cfg->mode == TG_SAMPLE && !uniforms) return TG_ERR_INVALID_ARGUMENT;
+  tg_status st = check_device(cfg);
+  if (st != TG_OK) return st;
+  // log-probabilities of a greedy config: the sampling kernel with the
+  // warpers off and u = 0 (its first token is the argmax, lowest index)
+  tg::DevCfg dev = cfg->dev;
+  if (out_logprobs && cfg->mode == TG_GREEDY) {
+    dev.mode = tg::kSample;
+    dev.temp = 1.0f;
+    dev.top_k = 0;
+    dev.top_p = 1.0f;
+    uniforms = nullptr;
+  }
+  tg::SelArgs a{};
+  a.logprobs = out_logprobs;
+  a.logits = logits;
+  a.nrows = B;
+  a.nrows_total = B;
+  a.V = V;
+  a.hist = hist_ids;
+  a.off = hist_offsets;
+  a.plen = prompt_lens;
+  a.uniforms = uniforms;
+  a.out = out_ids;
+  a.nwords = cfg->nwords;
+  const int grid = static_cast<int>(std::min<long long>(B, cfg->nsm));
+  return from_cuda(tg::launch_state(dev, a, grid, cfg->state_smem, reinterpret_cast<cudaStream_t>(stream),
+                                    state_ids, state_values));
 }
 
 tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_rows) {
@@ -399,7 +477,7 @@ tg_status tg_beam_step(const void* logits, int32_t num_prompts, int32_t num_beam
                        const float* beam_scores, const int32_t* hist_ids, const int64_t* hist_offsets,
                        const int32_t* prompt_lens, const tg_config* cfg, float* out_scores,
                        int32_t* out_tokens, int32_t* out_beams, tg_stream stream) {
-  if (!cfg || num_prompts < 0 || num_beams < 1 || V != cfg->V) return TG_ERR_INVALID_ARGUMENT;
+  if (!cfg || num_prompts < 0 || num_beams < 1 || V != cfg->V || cfg->dev.nproc > 0) return TG_ERR_INVALID_ARGUMENT;
   if (num_beams > tg::kMaxClusterBeams) return TG_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(num_prompts) * num_beams;
   if (rows > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;

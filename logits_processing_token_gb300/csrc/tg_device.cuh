@@ -34,6 +34,8 @@ constexpr unsigned kFlagBadId = 0x1u;
 constexpr unsigned kFlagBadRow = 0x2u;
 constexpr unsigned kFlagSlow = 0x4u;
 constexpr unsigned kFlagTimeout = 0x8u;
+constexpr unsigned kFlagBadState = 0x10u;
+constexpr int kMaxProcs = 8;           // the task's processors per config
 
 enum { kGreedy = 0, kSample = 1 };
 enum { kF32 = 0, kBF16 = 1 };
@@ -69,6 +71,20 @@ struct DevCfg {
   unsigned* status;
   unsigned long long* slow_rows;
   unsigned* tickets;
+  // The task's processors: kind (0 bias, 1 set) and state columns
+  // [pcol[k], pcol[k+1]) of processor k; pcol[nproc] = S.
+  int nproc;
+  int pkind[kMaxProcs];
+  int pcol[kMaxProcs + 1];
+  // Set per row on a thread-local copy by the kernels that take a state:
+  // prow routes process_elem through process_state_elem.
+  bool prow;
+  bool forced_row;              // a6/a7 active: the forced ids score 0, the rest F
+  int nfz;                      // forced ids left after a8/a9
+  int fz[8];
+  const int* pst_ids;           // this row's state (S columns), or null when dropped
+  const float* pst_vals;
+  const unsigned* pbits;        // bitmap of this row's state ids (shared memory)
 };
 
 struct SelArgs {
@@ -94,9 +110,12 @@ struct SelArgs {
 // Launch helpers (tg_kernels.cu).
 int select_smem_bytes(int nstage, int nwords);
 int process_smem_bytes(int nwords);
+int state_smem_bytes(int nwords);
 cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s);
 cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
-                           int smem, cudaStream_t s);
+                           int smem, cudaStream_t s, const int32_t* st_ids = nullptr, const float* st_vals = nullptr);
+cudaError_t launch_state(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s,
+                         const int32_t* st_ids, const float* st_vals);
 cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_sm);
 
 // Beam search, the device part of one step (tg_beam.cu).
@@ -519,12 +538,57 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
   return whole ? nl : -1;
 }
 
+// The task's processors (Transmuter.Generation, section "Processors") on one
+// token's score s, in list order: processor k finds t among the ids in use of
+// its state columns (ascending, -1 padding after them) by binary search; an
+// entry (t, v) makes s + v ("bias", one f32 add) or v ("set"), never below
+// the filter value.
+__device__ __forceinline__ float apply_state(const DevCfg& c, float s, int t) {
+  for (int k = 0; k < c.nproc; ++k) {
+    const int c0 = c.pcol[k], n = c.pcol[k + 1] - c0;
+    const int* ids = c.pst_ids + c0;
+    int lo = 0, hi = n;   // first column whose id is unused (-1) or >= t
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      const int v = __ldg(ids + mid);
+      if (v != -1 && v < t) lo = mid + 1; else hi = mid;
+    }
+    if (lo < n && __ldg(ids + lo) == t) {
+      const float v = __ldg(c.pst_vals + c0 + lo);
+      s = clampf(c.pkind[k] == 0 ? __fadd_rn(s, v) : v);
+    }
+  }
+  return s;
+}
+
+// a2-a9 and the task's processors for one token of a row that has a state
+// (or is forced): forced rows score 0 at the forced ids and F elsewhere;
+// other rows take the row bitmaps; then the processors, for tokens whose
+// bit is set in the row's state bitmap.
+static __device__ __noinline__ float process_state_elem(const DevCfg& c, const unsigned* H, const unsigned* N,
+                                                        float x, int i) {
+  float s;
+  if (c.forced_row) {
+    s = kFilter;
+    for (int q = 0; q < c.nfz; ++q) s = c.fz[q] == i ? 0.0f : s;
+  } else if (get_bit(N, i)) {
+    s = kFilter;
+  } else if (get_bit(H, i)) {
+    s = penalize(x, c.rho);
+  } else {
+    s = x;
+  }
+  if (c.pst_ids != nullptr && get_bit(c.pbits, i)) s = apply_state(c, s, i);
+  return s;
+}
+
 // Processed score of one token from its raw value and the row bitmaps
 // (a2-a9 for a row that is not forced), then temperature when sampling.
 __device__ __forceinline__ float process_elem(const DevCfg& c, const unsigned* H, const unsigned* N,
                                               float x, int i, bool sample) {
   float s = x;
-  if (get_bit(N, i)) s = kFilter;
+  if (c.prow) s = process_state_elem(c, H, N, x, i);
+  else if (get_bit(N, i)) s = kFilter;
   else if (get_bit(H, i)) s = penalize(x, c.rho);
   if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
   return s;

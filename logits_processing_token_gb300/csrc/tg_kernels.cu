@@ -1592,9 +1592,9 @@ struct SlowPick {
 template <int DT>
 __device__ __noinline__ SlowPick slow_select(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
                                              const unsigned char* rowp, unsigned* H, unsigned* N, bool bitmaps,
-                                             float u) {
+                                             float u, bool count = true) {
   csync();
-  if (threadIdx.x == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
+  if (count && threadIdx.x == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
   if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
   RowGlobalSource<DT> src{rowp, a.V, &c, H, N, bitmaps, true};
   float mm = -INFINITY;
@@ -2194,9 +2194,45 @@ struct ProcSmem {
   RedScratch red;
 };
 
+// The task's processors, once per row, every thread: check the row's state
+// (ids in [-1, V); within a processor's columns the ids in use ascend
+// strictly and the unused -1 come after them), set the bitmap P of its ids,
+// and fill the per-row fields of cr.  A state that breaks its layout is
+// dropped for the row and raises kFlagBadState.  P has nwords words.
+__device__ __forceinline__ void state_row_setup(DevCfg& cr, const RowMeta& rm, const int32_t* st_ids,
+                                                const float* st_vals, int row, unsigned* P, int nwords) {
+  const int S = cr.pcol[cr.nproc];
+  const int32_t* ids = st_ids + static_cast<size_t>(row) * S;
+  for (int w = threadIdx.x; w < nwords; w += kThreads) P[w] = 0u;
+  __syncthreads();
+  bool bad = false;
+  for (int j = threadIdx.x; j < S; j += kThreads) {
+    int end = S;
+    for (int k = 0; k < cr.nproc; ++k)
+      if (j < cr.pcol[k + 1]) { end = cr.pcol[k + 1]; break; }
+    const int t = __ldg(ids + j);
+    if (t < -1 || t >= cr.V) {
+      bad = true;
+    } else if (j + 1 < end) {
+      const int t2 = __ldg(ids + j + 1);
+      if (t == -1 ? t2 != -1 : (t2 != -1 && t2 <= t)) bad = true;
+    }
+    if (t >= 0 && t < cr.V) set_bit(P, t);
+  }
+  bad = __syncthreads_or(bad) != 0;
+  if (bad && threadIdx.x == 0) atomicOr(cr.status, kFlagBadState);
+  cr.prow = true;
+  cr.forced_row = rm.forced;
+  cr.nfz = rm.forced ? forced_zeros(cr, rm, cr.fz) : 0;
+  cr.pst_ids = bad ? nullptr : ids;
+  cr.pst_vals = bad ? nullptr : st_vals + static_cast<size_t>(row) * S;
+  cr.pbits = P;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
-    process_kernel(const DevCfg c, const SelArgs a, float* out_scores, unsigned* out_banbits, float* out_probs) {
+    process_kernel(const DevCfg c, const SelArgs a, float* out_scores, unsigned* out_banbits, float* out_probs,
+                   const int32_t* st_ids, const float* st_vals) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   ProcSmem& sm = *reinterpret_cast<ProcSmem*>(smem_raw);
   const int fixed = align_up(static_cast<int>(sizeof(ProcSmem)), 128);
@@ -2210,20 +2246,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rm.bad && threadIdx.x == 0) atomicOr(c.status, kFlagBadRow);
     return;
   }
+  DevCfg cr = c;
+  if (st_ids != nullptr) {
+    unsigned* P = reinterpret_cast<unsigned*>(smem_raw + fixed + 2 * bitmap_bytes(a.nwords));
+    state_row_setup(cr, rm, st_ids, st_vals, row, P, a.nwords);
+  }
   const void* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * (DT == kF32 ? 4 : 2);
   float* sc = out_scores + static_cast<size_t>(row) * V;
-  build_row_bitmaps(c, a.hist, rm, H, N, a.nwords);
+  build_row_bitmaps(cr, a.hist, rm, H, N, a.nwords);
   int zs[8];
   int nz = rm.forced ? forced_zeros(c, rm, zs) : 0;
   for (int i = threadIdx.x; i < V; i += kThreads) {
     float s;
-    if (rm.forced) {
+    if (rm.forced && !cr.prow) {
       s = kFilter;
       for (int q = 0; q < nz; ++q) if (zs[q] == i) s = 0.0f;
     } else {
       float x = DT == kF32 ? __ldg(static_cast<const float*>(rowp) + i)
                            : __uint_as_float(static_cast<unsigned>(__ldg(static_cast<const unsigned short*>(rowp) + i)) << 16);
-      s = process_elem(c, H, N, x, i, false);
+      s = process_elem(cr, H, N, x, i, false);
     }
     if (!c.renorm && sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
     sc[i] = s;
@@ -2289,6 +2330,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// state_kernel: tg_select_state, the selection with the task's processors
+// (Transmuter.Generation, section "Processors").  One CTA per row at a time
+// (grid-stride over the rows).  Per row: the state is checked and its ids set
+// in a bitmap P (in the space the TMA ring takes in select_kernel), the row
+// bitmaps are built, and every token is processed by process_elem, which
+// takes the processor path (forced rows included).  Greedy: one pass, block
+// argmax (lowest index on ties).  Sampling: the exact multi-pass selection
+// of select_kernel's slow path (row maximum, fixed-point mass, top_k / top_p
+// cut and draw by value windows or radix selection), uncounted.
+// ---------------------------------------------------------------------------
+template <int DT, bool SAMPLE>
+__global__ void __launch_bounds__(kThreads, 1)
+    state_kernel(const DevCfg c, const SelArgs a, const int32_t* st_ids, const float* st_vals) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  unsigned* H = reinterpret_cast<unsigned*>(smem_raw + fin_offset());
+  unsigned* N = H + bitmap_bytes(a.nwords) / 4;
+  unsigned* P = reinterpret_cast<unsigned*>(smem_raw + ring_offset(a.nwords));
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int V = a.V;
+  constexpr int esz = DT == kF32 ? 4 : 2;
+  for (int row = blockIdx.x; row < a.nrows; row += gridDim.x) {
+    const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
+    if (rm.bad || rm.L == 0) {
+      if (tid == 0) {
+        a.out[row] = -1;
+        if (SAMPLE && a.logprobs) a.logprobs[row] = __int_as_float(0x7fc00000);
+        if (rm.bad) atomicOr(c.status, kFlagBadRow);
+      }
+      continue;
+    }
+    DevCfg cr = c;
+    state_row_setup(cr, rm, st_ids, st_vals, row, P, a.nwords);
+    build_row_bitmaps(cr, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+    const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
+    if (!SAMPLE) {
+      const RowGlobalSource<DT> src{rowp, V, &cr, H, N, true, false};
+      float bv = -INFINITY;
+      unsigned bi = 0xffffffffu;
+      src.pass([&](float s, unsigned i) {
+        if (s > bv || (s == bv && i < bi)) { bv = s; bi = i; }
+      });
+      for (int o = 16; o; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const unsigned i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (v2 > bv || (v2 == bv && i2 < bi)) { bv = v2; bi = i2; }
+      }
+      csync();
+      if (lane == 0) { sm.misc.wf[wid] = bv; sm.misc.wu[wid] = bi; }
+      csync();
+      if (tid == 0) {
+        float v = sm.misc.wf[0];
+        unsigned b = sm.misc.wu[0];
+        for (int q = 1; q < kWarps; ++q) {
+          const float v2 = sm.misc.wf[q];
+          const unsigned i2 = sm.misc.wu[q];
+          if (v2 > v || (v2 == v && i2 < b)) { v = v2; b = i2; }
+        }
+        a.out[row] = static_cast<int>(b);
+      }
+    } else {
+      const float u = a.uniforms ? a.uniforms[row] : 0.0f;
+      const SlowPick sp = slow_select<DT>(cr, a, sm, rm, rowp, H, N, true, u, false);
+      if (tid == 0) {
+        a.out[row] = static_cast<int>(sp.token);
+        if (a.logprobs) a.logprobs[row] = token_logprob(sp.score, sp.ref, sp.fast, sp.S);
+      }
+    }
+    __syncthreads();
+  }
+}
 
 // ---------------------------------------------------------------------------
 // host-side launch helpers (C++ linkage, used by tg_api.cu)
@@ -2417,8 +2531,10 @@ namespace tg {
 
 int select_smem_bytes(int nstage, int nwords) { return ring_offset(nwords) + nstage * kStageBytes; }
 int process_smem_bytes(int nwords) {
-  return align_up(static_cast<int>(sizeof(ProcSmem)), 128) + 2 * bitmap_bytes(nwords);
+  // the row bitmaps and the state bitmap
+  return align_up(static_cast<int>(sizeof(ProcSmem)), 128) + 3 * bitmap_bytes(nwords);
 }
+int state_smem_bytes(int nwords) { return ring_offset(nwords) + bitmap_bytes(nwords); }
 
 // One launch per kMaxRowsPerCta * grid rows; each is a programmatic dependent
 // of the kernel before it in the stream (its launch overlaps that kernel's
@@ -2466,18 +2582,39 @@ cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int gr
 }
 
 cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
-                           int smem, cudaStream_t s) {
+                           int smem, cudaStream_t s, const int32_t* st_ids, const float* st_vals) {
   cudaError_t e;
   if (c.dtype == kF32) {
     e = cudaFuncSetAttribute(process_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    process_kernel<kF32><<<a.nrows, kThreads, smem, s>>>(c, a, scores, banbits, probs);
+    process_kernel<kF32><<<a.nrows, kThreads, smem, s>>>(c, a, scores, banbits, probs, st_ids, st_vals);
   } else {
     e = cudaFuncSetAttribute(process_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    process_kernel<kBF16><<<a.nrows, kThreads, smem, s>>>(c, a, scores, banbits, probs);
+    process_kernel<kBF16><<<a.nrows, kThreads, smem, s>>>(c, a, scores, banbits, probs, st_ids, st_vals);
   }
   return cudaGetLastError();
+}
+
+template <int DT, bool SAMPLE>
+static cudaError_t launch_state_t(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s,
+                                  const int32_t* st_ids, const float* st_vals) {
+  auto k = state_kernel<DT, SAMPLE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, s>>>(c, a, st_ids, st_vals);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_state(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s,
+                         const int32_t* st_ids, const float* st_vals) {
+  if (grid < 1) return cudaErrorInvalidValue;
+  const bool sample = c.mode == kSample;
+  if (c.dtype == kF32)
+    return sample ? launch_state_t<kF32, true>(c, a, grid, smem, s, st_ids, st_vals)
+                  : launch_state_t<kF32, false>(c, a, grid, smem, s, st_ids, st_vals);
+  return sample ? launch_state_t<kBF16, true>(c, a, grid, smem, s, st_ids, st_vals)
+                : launch_state_t<kBF16, false>(c, a, grid, smem, s, st_ids, st_vals);
 }
 
 cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_sm) {

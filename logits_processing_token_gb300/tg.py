@@ -25,13 +25,17 @@ TG_GREEDY, TG_SAMPLE = 0, 1
 TG_FLAG_HISTORY_ID_OUT_OF_RANGE = 0x1
 TG_FLAG_BAD_ROW = 0x2
 TG_FLAG_SLOW_PATH = 0x4
+TG_FLAG_BAD_STATE = 0x10
 TG_MAX_VOCAB = 1 << 18
+TG_PROC_BIAS, TG_PROC_SET = 0, 1
+TG_MAX_PROCESSORS = 8
+TG_MAX_STATE_COLS = 4096
 
 # Names of every entry point declared in include/tg.h.
 EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
            "tg_status_string", "tg_verify_noalloc", "tg_beam_step", "tg_beam_keep",
-           "tg_verify_history")
+           "tg_verify_history", "tg_select_state", "tg_process_state")
 TG_NOALLOC_MAX_BATCH = 1024
 
 
@@ -70,6 +74,9 @@ class tg_params(ctypes.Structure):
         ("bad_word_seq_offsets", POINTER(c_int32)),
         ("n_bad_word_seqs", c_int32),
         ("renormalize_logits", c_int32),
+        ("processor_kinds", POINTER(c_int32)),
+        ("processor_sizes", POINTER(c_int32)),
+        ("n_processors", c_int32),
     ]
 
 
@@ -107,6 +114,12 @@ def load_library(path: str | None = None):
     lib.tg_verify_noalloc.restype = c_int
     lib.tg_process.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_void_p]
+    lib.tg_select_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.tg_select_state.restype = c_int
+    lib.tg_process_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.tg_process_state.restype = c_int
     lib.tg_query_status.argtypes = [c_void_p, POINTER(c_uint32), POINTER(c_uint64)]
     lib.tg_clear_status.argtypes = [c_void_p]
     lib.tg_beam_step.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -144,7 +157,7 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
                 no_repeat_ngram_size=0, bad_words_ids=(), suppress_tokens=(), begin_suppress_tokens=(),
                 eos_token_ids=(), min_length=0, min_new_tokens=0, forced_bos_token_id=-1,
                 forced_eos_token_ids=(), max_new_tokens=0, temperature=1.0, top_k=0, top_p=1.0,
-                max_batch=0, bad_word_seqs=(), renormalize_logits=False):
+                max_batch=0, bad_word_seqs=(), renormalize_logits=False, processors=()):
     """A filled tg_params plus the ctypes arrays its pointers refer to."""
     lib = load_library()
     p = tg_params()
@@ -183,6 +196,16 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
         p.bad_word_seq_ids = ctypes.cast(ids_arr, POINTER(c_int32))
         p.bad_word_seq_offsets = ctypes.cast(off_arr, POINTER(c_int32))
         p.n_bad_word_seqs = len(seqs)
+    # the task's processors: (kind, size) pairs, kind "bias" / "set" or TG_PROC_*
+    procs = [(({"bias": TG_PROC_BIAS, "set": TG_PROC_SET}[k] if isinstance(k, str) else int(k)), int(n))
+             for k, n in processors]
+    if procs:
+        kinds_arr, _ = _ids([k for k, _ in procs])
+        sizes_arr, _ = _ids([n for _, n in procs])
+        keep += [kinds_arr, sizes_arr]
+        p.processor_kinds = ctypes.cast(kinds_arr, POINTER(c_int32))
+        p.processor_sizes = ctypes.cast(sizes_arr, POINTER(c_int32))
+        p.n_processors = len(procs)
     return p, keep
 
 
@@ -283,6 +306,63 @@ def tg_select(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, uniforms
         st = lib.tg_select_logprobs(*args, _ptr(out_logprobs, "out_logprobs", (torch.float32,)), _stream(stream))
         _check("tg_select_logprobs", st)
     return out_ids
+
+
+def _state_cols(cfg):
+    return sum(int(n) for _, n in cfg.params.get("processors", ()))
+
+
+def tg_select_state(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, state_ids, state_values, uniforms,
+                    out_ids, out_logprobs=None, stream=None):
+    """tg_select with the config's task processors: state_ids int32 [B, S] and state_values f32
+    [B, S] (S = the processors' columns); out_logprobs [B] f32 or None."""
+    import torch
+    _need(logits.dim() == 2, "logits must be [B, V]")
+    _check_logits(logits, cfg, "logits")
+    B, V = int(logits.shape[0]), int(logits.shape[-1])
+    S = _state_cols(cfg)
+    _check_len(hist_offsets, B + 1, "hist_offsets")
+    _check_len(prompt_lens, B, "prompt_lens")
+    _check_len(state_ids, B * S, "state_ids")
+    _check_len(state_values, B * S, "state_values")
+    _check_len(uniforms, B, "uniforms")
+    _check_len(out_ids, B, "out_ids")
+    _check_len(out_logprobs, B, "out_logprobs")
+    st = load_library().tg_select_state(
+        _ptr(logits, "logits", _logit_dtypes()), B, V,
+        _ptr(hist_ids, "hist_ids", (torch.int32,), allow_none=True) if hist_ids is not None and hist_ids.numel() else None,
+        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+        cfg.handle, _ptr(state_ids, "state_ids", (torch.int32,)), _ptr(state_values, "state_values", (torch.float32,)),
+        _ptr(uniforms, "uniforms", (torch.float32,), allow_none=True), _ptr(out_ids, "out_ids", (torch.int32,)),
+        _ptr(out_logprobs, "out_logprobs", (torch.float32,), allow_none=True), _stream(stream))
+    _check("tg_select_state", st)
+    return out_ids
+
+
+def tg_process_state(logits, hist_ids, hist_offsets, prompt_lens, cfg: Config, state_ids, state_values, out_scores,
+                     out_banbits=None, out_probs=None, stream=None):
+    """tg_process with the config's task processors (state as tg_select_state)."""
+    import torch
+    _need(logits.dim() == 2, "logits must be [B, V]")
+    _check_logits(logits, cfg, "logits")
+    B, V = int(logits.shape[0]), int(logits.shape[-1])
+    S = _state_cols(cfg)
+    _check_len(hist_offsets, B + 1, "hist_offsets")
+    _check_len(prompt_lens, B, "prompt_lens")
+    _check_len(state_ids, B * S, "state_ids")
+    _check_len(state_values, B * S, "state_values")
+    _check_len(out_scores, B * V, "out_scores")
+    _check_len(out_banbits, B * ((V + 31) // 32), "out_banbits")
+    _check_len(out_probs, B * V, "out_probs")
+    st = load_library().tg_process_state(
+        _ptr(logits, "logits", _logit_dtypes()), B, V,
+        _ptr(hist_ids, "hist_ids", (torch.int32,)) if hist_ids is not None and hist_ids.numel() else None,
+        _ptr(hist_offsets, "hist_offsets", (torch.int64,)), _ptr(prompt_lens, "prompt_lens", (torch.int32,)),
+        cfg.handle, _ptr(state_ids, "state_ids", (torch.int32,)), _ptr(state_values, "state_values", (torch.float32,)),
+        _ptr(out_scores, "out_scores", (torch.float32,)),
+        _ptr(out_banbits, "out_banbits", (torch.int32, torch.uint32), allow_none=True),
+        _ptr(out_probs, "out_probs", (torch.float32,), allow_none=True), _stream(stream))
+    _check("tg_process_state", st)
 
 
 def tg_beam_keep(cfg: Config, num_beams: int) -> int:

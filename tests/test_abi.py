@@ -133,3 +133,34 @@ def test_binding_rejects_mis_shaped_tensors():
     with pytest.raises(ValueError, match="out_scores"):
         tg.tg_process(torch.zeros(2, 64), None, torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=i32),
                       cfg32, torch.zeros(2, 63))
+
+
+def test_config_create_rejects_bad_processors_on_host(lib):
+    # the task's processors: kind bias/set, sizes >= 1, at most 8 of them and 4,096 columns in all
+    bad = [dict(processors=[(2, 4)]), dict(processors=[("bias", 0)]),
+           dict(processors=[("bias", 1)] * (tg.TG_MAX_PROCESSORS + 1)),
+           dict(processors=[("bias", tg.TG_MAX_STATE_COLS), ("set", 1)])]
+    for kw in bad:
+        p, keep = tg.make_params(vocab=10, **kw)
+        h = ctypes.c_void_p()
+        assert lib.tg_config_create(ctypes.byref(p), ctypes.byref(h)) == tg.TG_ERR_INVALID_ARGUMENT, kw
+
+
+def test_state_entry_points_reject_null_arguments(lib):
+    assert lib.tg_select_state(None, 1, 10, None, None, None, None, None, None, None, None, None,
+                               None) == tg.TG_ERR_INVALID_ARGUMENT
+    assert lib.tg_process_state(None, 1, 10, None, None, None, None, None, None, None, None, None,
+                                None) == tg.TG_ERR_INVALID_ARGUMENT
+
+
+def test_binding_checks_the_state_shape():
+    import types
+    import torch
+    cfg = types.SimpleNamespace(params=dict(vocab=64, logits_dtype="f32", processors=[("bias", 3), ("set", 2)]),
+                                handle=None)
+    i32 = torch.int32
+    args = (torch.zeros(2, 64), None, torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=i32), cfg)
+    with pytest.raises(ValueError, match="state_ids"):
+        tg.tg_select_state(*args, torch.zeros(2, 4, dtype=i32), torch.zeros(2, 5), None, torch.zeros(2, dtype=i32))
+    with pytest.raises(ValueError, match="state_values"):
+        tg.tg_process_state(*args, torch.zeros(2, 5, dtype=i32), torch.zeros(2, 4), torch.zeros(2, 64))
