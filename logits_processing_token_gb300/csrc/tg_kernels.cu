@@ -210,7 +210,26 @@ struct RowGlobalSource {
   const unsigned* N;
   bool bitmaps;
   bool sample;
+  // rows with the task's processors (state_kernel): P marks the state ids
+  // and forced ids; a token in neither H nor P is plain (or F when forced)
+  bool prow = false;
+  bool forced = false;
+  const unsigned* P = nullptr;
+  float temp = 1.0f;
+  __device__ __forceinline__ void state_row(const DevCfg& cr) {
+    prow = cr.prow;
+    forced = cr.forced_row;
+    P = cr.pbits;
+    temp = cr.temp;
+  }
   __device__ __forceinline__ float score(float x, int i) const {
+    if (prow) {
+      float s;
+      if (get_bit(H, i) || get_bit(P, i)) s = process_state_elem(*c, H, N, x, i);
+      else s = forced ? kFilter : x;
+      if (sample && temp != 1.0f) s = clampf(__fdiv_rn(s, temp));
+      return s;
+    }
     if (bitmaps) return process_elem(*c, H, N, x, i, sample);
     if (sample && c->temp != 1.0f) return clampf(__fdiv_rn(x, c->temp));
     return x;
@@ -1597,6 +1616,7 @@ __device__ __noinline__ SlowPick slow_select(const DevCfg& c, const SelArgs& a, 
   if (count && threadIdx.x == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
   if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
   RowGlobalSource<DT> src{rowp, a.V, &c, H, N, bitmaps, true};
+  if (c.prow) src.state_row(c);
   float mm = -INFINITY;
   src.pass([&](float s, unsigned) { mm = fmaxf(mm, s); });
   mm = block_max(mm, &sm.red);
@@ -2196,8 +2216,9 @@ struct ProcSmem {
 
 // The task's processors, once per row, every thread: check the row's state
 // (ids in [-1, V); within a processor's columns the ids in use ascend
-// strictly and the unused -1 come after them), set the bitmap P of its ids,
-// and fill the per-row fields of cr.  A state that breaks its layout is
+// strictly and the unused -1 come after them), set the bitmap P of its ids
+// and of a forced row's forced ids (a token outside P and the row bitmaps
+// needs no processing), and fill the per-row fields of cr.  A state that breaks its layout is
 // dropped for the row and raises kFlagBadState.  P has nwords words.
 __device__ __forceinline__ void state_row_setup(DevCfg& cr, const RowMeta& rm, const int32_t* st_ids,
                                                 const float* st_vals, int row, unsigned* P, int nwords) {
@@ -2224,6 +2245,8 @@ __device__ __forceinline__ void state_row_setup(DevCfg& cr, const RowMeta& rm, c
   cr.prow = true;
   cr.forced_row = rm.forced;
   cr.nfz = rm.forced ? forced_zeros(cr, rm, cr.fz) : 0;
+  if (threadIdx.x < cr.nfz) set_bit(P, cr.fz[threadIdx.x]);
+  __syncthreads();
   cr.pst_ids = bad ? nullptr : ids;
   cr.pst_vals = bad ? nullptr : st_vals + static_cast<size_t>(row) * S;
   cr.pbits = P;
@@ -2368,7 +2391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     build_row_bitmaps(cr, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
     if (!SAMPLE) {
-      const RowGlobalSource<DT> src{rowp, V, &cr, H, N, true, false};
+      RowGlobalSource<DT> src{rowp, V, &cr, H, N, true, false};
+      src.state_row(cr);
       float bv = -INFINITY;
       unsigned bi = 0xffffffffu;
       src.pass([&](float s, unsigned i) {
