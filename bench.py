@@ -453,6 +453,7 @@ def run_state(args):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    tg.tg_clear_status(cfg)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -461,6 +462,7 @@ def run_state(args):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
+    flags, slow_rows = tg.tg_query_status(cfg)
     peak, peak_kind = measured_peak()
     alg, _ = required_bytes(w)
     alg += int(st_ids.size) * 8
@@ -473,8 +475,10 @@ def run_state(args):
                        "l2": "inputs rotate over %d copies of the logits > L2" % n_sets},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": "%s hbm_gbs (copy)" % peak_kind,
-                         "bytes_per_launch": alg, "kernel": "state_kernel<bf16>", "traffic": None},
-            "gpu_launches": args.steps}
+                         "bytes_per_step": alg,
+                         "kernel": "select_kernel<bf16> (state ids marked), then state_kernel<bf16> on the rows it "
+                                   "defers (forced rows here)", "traffic": None},
+            "gpu_launches": 2 * args.steps, "slow_path_rows": slow_rows, "status_flags": flags}
     print(json.dumps(line), flush=True)
 
 

@@ -231,8 +231,15 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
 
   st = plan_select(c.dtype, false, cfg->nwords, &cfg->sel);
   if (st == TG_OK) st = plan_select(c.dtype, true, 0, &cfg->ver);
-  cfg->proc_smem = tg::process_smem_bytes(cfg->nwords);
-  cfg->state_smem = tg::state_smem_bytes(cfg->nwords);
+  cfg->proc_smem = tg::process_smem_bytes(cfg->nwords, c.pcol[c.nproc]);
+  cfg->state_smem = tg::state_smem_bytes(cfg->nwords, c.pcol[c.nproc]);
+  if (st == TG_OK && c.nproc > 0) {
+    // the state kernels stage the state in shared memory: it must fit
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, cfg->device);
+    if (e != cudaSuccess) st = from_cuda(e);
+    else if (cfg->state_smem > optin || cfg->proc_smem > optin) st = TG_ERR_UNSUPPORTED;
+  }
   if (st != TG_OK) {
     cudaFree(cfg->dmem);
     delete cfg;
@@ -438,6 +445,15 @@ tg_status tg_select_state(const void* logits, int32_t B, int32_t V, const int32_
   a.uniforms = uniforms;
   a.out = out_ids;
   a.nwords = cfg->nwords;
+  a.st_ids = state_ids;
+  a.st_vals = state_values;
+  // select_kernel finishes the rows its one-pass path can (the state ids are
+  // marked tokens there) and leaves the rest to state_kernel
+  a.nstage = cfg->sel.nstage;
+  const int grid_sel = static_cast<int>(std::min<long long>(B, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm));
+  cudaError_t e = tg::launch_select(dev, a, false, grid_sel, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e);
+  a.fixup = 1;
   const int grid = static_cast<int>(std::min<long long>(B, cfg->nsm));
   return from_cuda(tg::launch_state(dev, a, grid, cfg->state_smem, reinterpret_cast<cudaStream_t>(stream),
                                     state_ids, state_values));

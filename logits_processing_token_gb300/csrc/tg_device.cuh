@@ -85,6 +85,10 @@ struct DevCfg {
   const int* pst_ids;           // this row's state (S columns), or null when dropped
   const float* pst_vals;
   const unsigned* pbits;        // bitmap of this row's state ids (shared memory)
+  bool sparse_row;              // forced row with a state: only the pbits tokens can score above F
+  const float* sp_s;            // a sparse row's tokens above F: processed scores and ids (shared memory)
+  const unsigned* sp_i;
+  int sp_n;
 };
 
 struct SelArgs {
@@ -105,12 +109,18 @@ struct SelArgs {
   float* logprobs;       // select: the token's log-probability per row, or null
   int nstage;
   int nwords;
+  // the task's processors (tg_select_state): row b's state is st_ids/st_vals[b*S .. b*S+S)
+  const int32_t* st_ids;
+  const float* st_vals;
+  int fixup;             // state_kernel: only rows select_kernel deferred (out == kDeferred)
 };
+// select_kernel with a state leaves this id for the rows it hands to state_kernel.
+constexpr int kDeferred = -2;
 
 // Launch helpers (tg_kernels.cu).
 int select_smem_bytes(int nstage, int nwords);
-int process_smem_bytes(int nwords);
-int state_smem_bytes(int nwords);
+int process_smem_bytes(int nwords, int S);
+int state_smem_bytes(int nwords, int S);
 cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s);
 cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
                            int smem, cudaStream_t s, const int32_t* st_ids = nullptr, const float* st_vals = nullptr);
@@ -400,9 +410,16 @@ __device__ __forceinline__ bool get_bit(const unsigned* bm, int t) { return (bm[
 // value is -1 when no list is made (not asked for, history not staged, or
 // more marked tokens than fit), and N keeps the bitmap.
 constexpr unsigned kBannedFlag = 0x80000000u;
+constexpr unsigned kPlainFlag = 0x40000000u;   // listed from the processors' state only: no penalty
+constexpr unsigned kIdMask = 0x3fffffffu;
+//
+// With `sids` (S ids of a row's processor state, -1 unused), the state ids
+// are marked too and listed last: a state id that is no history id and not
+// banned gets kPlainFlag (its score is x before the processors).
 static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int32_t* hist, const RowMeta& r,
                                                      unsigned* H, unsigned* N, int nwords, int* stage = nullptr,
-                                                     int stage_cap = 0, unsigned* ctr = nullptr) {
+                                                     int stage_cap = 0, unsigned* ctr = nullptr,
+                                                     const int32_t* sids = nullptr, int S = 0) {
   const int tid = threadIdx.x;
   for (int w = tid; w < nwords; w += kThreads) { H[w] = 0u; N[w] = 0u; }
   const int V = c.V;
@@ -475,6 +492,10 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
   if (r.bsup)
     for (int i = tid; i < c.n_bsup; i += kThreads) set_bit(N, __ldg(c.bsup_sorted + i));
   if (bad_id) atomicOr(c.status, kFlagBadId);
+  for (int j = tid; j < S; j += kThreads) {
+    const int t = __ldg(sids + j);
+    if (t >= 0 && t < V) set_bit(H, t);
+  }
   const bool listing = ctr != nullptr && staged;
   if (listing && tid == 0) *ctr = 0u;
   csync();
@@ -503,13 +524,13 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
   csync();
   int* tmp = stage + L;
   const int lane = tid & 31;
-  auto claim = [&](int t) {   // every lane of the warp calls, t < 0 for none
+  auto claim = [&](int t, unsigned extra = 0u) {   // every lane of the warp calls, t < 0 for none
     bool own = false;
     unsigned e = 0u;
     if (t >= 0 && t < V) {
       const unsigned bit = 1u << (t & 31);
       own = (atomicAnd(&H[t >> 5], ~bit) & bit) != 0u;
-      e = static_cast<unsigned>(t) | ((N[t >> 5] & bit) ? kBannedFlag : 0u);
+      e = static_cast<unsigned>(t) | ((N[t >> 5] & bit) ? kBannedFlag : extra);
     }
     const unsigned bal = __ballot_sync(0xffffffffu, own);
     if (bal) {
@@ -526,13 +547,15 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
   if (r.eos_off) claim(tid < c.n_eos ? c.eos[tid] : -1);
   if (r.bsup)
     for (int i0 = 0; i0 < c.n_bsup; i0 += kThreads) claim(i0 + tid < c.n_bsup ? __ldg(c.bsup_sorted + i0 + tid) : -1);
+  // last: what is still unclaimed of the state is neither history nor banned
+  for (int i0 = 0; i0 < S; i0 += kThreads) claim(i0 + tid < S ? __ldg(sids + i0 + tid) : -1, kPlainFlag);
   csync();
   const int nl = static_cast<int>(*ctr);
   const bool whole = nl == total;   // always, unless a marked token had no source
   for (int i = tid; i < nl; i += kThreads) {
     const unsigned e = static_cast<unsigned>(tmp[i]);
     if (whole) N[i] = e;
-    atomicOr(&H[(e & ~kBannedFlag) >> 5], 1u << (e & 31u));
+    atomicOr(&H[(e & kIdMask) >> 5], 1u << (e & 31u));
   }
   csync();
   return whole ? nl : -1;
@@ -542,23 +565,27 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
 // token's score s, in list order: processor k finds t among the ids in use of
 // its state columns (ascending, -1 padding after them) by binary search; an
 // entry (t, v) makes s + v ("bias", one f32 add) or v ("set"), never below
-// the filter value.
-__device__ __forceinline__ float apply_state(const DevCfg& c, float s, int t) {
+// the filter value.  The state may be in global or shared memory.
+__device__ __forceinline__ float apply_state_at(const DevCfg& c, const int* sids, const float* svals, float s,
+                                                int t) {
   for (int k = 0; k < c.nproc; ++k) {
     const int c0 = c.pcol[k], n = c.pcol[k + 1] - c0;
-    const int* ids = c.pst_ids + c0;
+    const int* ids = sids + c0;
     int lo = 0, hi = n;   // first column whose id is unused (-1) or >= t
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      const int v = __ldg(ids + mid);
+      const int v = ids[mid];
       if (v != -1 && v < t) lo = mid + 1; else hi = mid;
     }
-    if (lo < n && __ldg(ids + lo) == t) {
-      const float v = __ldg(c.pst_vals + c0 + lo);
+    if (lo < n && ids[lo] == t) {
+      const float v = svals[c0 + lo];
       s = clampf(c.pkind[k] == 0 ? __fadd_rn(s, v) : v);
     }
   }
   return s;
+}
+__device__ __forceinline__ float apply_state(const DevCfg& c, float s, int t) {
+  return apply_state_at(c, c.pst_ids, c.pst_vals, s, t);
 }
 
 // a2-a9 and the task's processors for one token of a row that has a state
@@ -599,6 +626,26 @@ __device__ __forceinline__ float process_elem(const DevCfg& c, const unsigned* H
 // sampling.  The same result as process_elem for such a token.
 __device__ __forceinline__ float process_marked(const DevCfg& c, float x, bool banned, bool sample) {
   float s = banned ? kFilter : penalize(x, c.rho);
+  if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
+  return s;
+}
+
+// A 1,024-bit filter of a row's state ids (bit t mod 1024): a token whose bit
+// is clear is no state id.
+constexpr int kStateFilterWords = 32;
+__device__ __forceinline__ bool state_filter_hit(const unsigned* f, int t) {
+  return (f[(t >> 5) & (kStateFilterWords - 1)] >> (t & 31)) & 1u;
+}
+
+// Processed score of a listed marked token from its raw value and its list
+// entry e (banned, plain or a penalised history id), then the row's processor
+// state when sids is given (sfilt: the state ids' filter), then temperature
+// when sampling.
+__device__ __forceinline__ float process_listed(const DevCfg& c, float x, unsigned e, const int* sids,
+                                                const float* svals, const unsigned* sfilt, bool sample) {
+  float s = (e & kBannedFlag) ? kFilter : ((e & kPlainFlag) ? x : penalize(x, c.rho));
+  const int t = static_cast<int>(e & kIdMask);
+  if (sids != nullptr && state_filter_hit(sfilt, t)) s = apply_state_at(c, sids, svals, s, t);
   if (sample && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
   return s;
 }

@@ -137,6 +137,7 @@ struct Misc {
   float wf[kWarps];                      // per-warp scratch
   unsigned wu[kWarps];
   unsigned lvl[kWarps][4];               // first sub-chunk: packed counts per level of 2 below m0
+  unsigned sfilt[kStateFilterWords];     // the row's state ids, as a 1,024-bit filter
 };
 
 constexpr int kLevels = 1024;   // value levels between the lowest candidate and the row max
@@ -214,13 +215,21 @@ struct RowGlobalSource {
   // and forced ids; a token in neither H nor P is plain (or F when forced)
   bool prow = false;
   bool forced = false;
+  bool sparse = false;   // a forced row: only its tokens above F (final scores, listed once)
   const unsigned* P = nullptr;
   float temp = 1.0f;
+  const float* sp_s = nullptr;
+  const unsigned* sp_i = nullptr;
+  int sp_n = 0;
   __device__ __forceinline__ void state_row(const DevCfg& cr) {
     prow = cr.prow;
     forced = cr.forced_row;
+    sparse = cr.sparse_row;
     P = cr.pbits;
     temp = cr.temp;
+    sp_s = cr.sp_s;
+    sp_i = cr.sp_i;
+    sp_n = cr.sp_n;
   }
   __device__ __forceinline__ float score(float x, int i) const {
     if (prow) {
@@ -239,6 +248,11 @@ struct RowGlobalSource {
   // unaligned row element by element.
   template <class Fn>
   __device__ __forceinline__ void pass(Fn f) const {
+    if (sparse) {
+      // every other token scores F and weighs nothing: the listed ones only
+      for (int j = threadIdx.x; j < sp_n; j += kThreads) f(sp_s[j], sp_i[j]);
+      return;
+    }
     constexpr int PER = DT == kF32 ? 4 : 8;
     constexpr int NV = 4;
     int done = 0;
@@ -411,8 +425,9 @@ __device__ __forceinline__ void walk_sorted(SelSmem& sm, int cnt, unsigned long 
   csync();
 }
 
-// End of a row, listed marked tokens: entry j of list[0..n) (t | banned
-// << 31) is read back from global memory and passed to fn(x, t, banned, j).
+// End of a row, listed marked tokens: entry j of list[0..n) (t and the
+// banned / plain flags) is read back from global memory and passed to
+// fn(x, t, entry, j).
 // Thread t takes entries t, t + kThreads, ... four at a time with the four
 // reads in flight.
 template <int DT, class Fn>
@@ -427,11 +442,11 @@ __device__ __forceinline__ void for_listed(const unsigned* list, int n, const un
       e[q] = j < n ? list[j] : 0xffffffffu;
     }
 #pragma unroll
-    for (int q = 0; q < kMB; ++q) xs[q] = e[q] != 0xffffffffu ? load_logit<DT>(rowp, static_cast<int>(e[q] & ~kBannedFlag)) : 0.0f;
+    for (int q = 0; q < kMB; ++q) xs[q] = e[q] != 0xffffffffu ? load_logit<DT>(rowp, static_cast<int>(e[q] & kIdMask)) : 0.0f;
 #pragma unroll
     for (int q = 0; q < kMB; ++q)
       if (e[q] != 0xffffffffu)
-        fn(xs[q], static_cast<int>(e[q] & ~kBannedFlag), (e[q] & kBannedFlag) != 0u, j0 + q * kThreads + static_cast<int>(threadIdx.x));
+        fn(xs[q], static_cast<int>(e[q] & kIdMask), e[q], j0 + q * kThreads + static_cast<int>(threadIdx.x));
   }
 }
 
@@ -1614,18 +1629,22 @@ __device__ __noinline__ SlowPick slow_select(const DevCfg& c, const SelArgs& a, 
                                              float u, bool count = true) {
   csync();
   if (count && threadIdx.x == 0) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
+  TG_TF(15);
   if (bitmaps) build_row_bitmaps(c, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+  TG_TF(16);
   RowGlobalSource<DT> src{rowp, a.V, &c, H, N, bitmaps, true};
   if (c.prow) src.state_row(c);
   float mm = -INFINITY;
   src.pass([&](float s, unsigned) { mm = fmaxf(mm, s); });
   mm = block_max(mm, &sm.red);
+  TG_TF(17);
   const bool topk = c.top_k > 0 && static_cast<unsigned>(c.top_k) < static_cast<unsigned>(a.V);
   if (!topk && mm > kFilter) {
     unsigned long long z_t = 0ull;
     const WFast wz{mm * kLog2e};
     src.pass([&](float s, unsigned) { z_t += wz(s); });
     const unsigned long long Z = block_sum_u64(z_t, &sm.red);
+    TG_TF(18);
     unsigned long long S = Z;
     bool ok = Z > 0ull;
     // an exact pick over a window uses the finishing area, which holds the
@@ -1635,12 +1654,15 @@ __device__ __noinline__ SlowPick slow_select(const DevCfg& c, const SelArgs& a, 
     };
     if (ok && c.top_p < 1.0f) {
       const LevelPick cut = level_pick<DT>(src, sm, mm, Z, topp_target(c.top_p, Z), false);
+      TG_TF(19);
       restore();
+      TG_TF(20);
       ok = cut.ok;
       S = cut.cum;
     }
     if (ok) {
       const LevelPick d = level_pick<DT>(src, sm, mm, Z, draw_target(u, S), true);
+      TG_TF(21);
       if (d.ok) return SlowPick{d.idx, key2f(d.key), mm * kLog2e, true, S};
     }
     restore();
@@ -1700,19 +1722,28 @@ __device__ __forceinline__ void verify_ticket(const DevCfg& c, const SelArgs& a,
 // Forced rows do not depend on the logits: the forced ids score 0, all
 // others the filter value; greedy takes the lowest, sampling draws among them.
 // *kept = how many equal-scored tokens the step selects from.
-__device__ __forceinline__ int forced_token(const DevCfg& c, const RowMeta& rm, int V, float u, bool sample,
-                                            unsigned long long* kept) {
-  int zs[8];
-  const int nz = forced_zeros(c, rm, zs);
-  const unsigned long long cnt = nz ? static_cast<unsigned long long>(nz) : static_cast<unsigned long long>(V);
+// Among cnt equal-scored tokens in index order: greedy takes the first;
+// sampling keeps the top-p prefix and draws in it.  Returns the position;
+// *kept = the tokens the step selects from.
+__device__ __forceinline__ int equal_pick(const DevCfg& c, unsigned long long cnt, float u, bool sample,
+                                          unsigned long long* kept) {
   *kept = cnt;
-  if (!sample) return nz ? zs[0] : 0;
+  if (!sample) return 0;
   const unsigned long long W = 1ull << kFixShift;
   unsigned long long ncut = cnt;
   if (c.top_p < 1.0f) ncut = group_pick(0ull, W, cnt, topp_target(c.top_p, cnt * W), false);
   *kept = ncut;
   const unsigned long long nd = group_pick(0ull, W, ncut, draw_target(u, ncut * W), true);
-  return nz ? zs[nd - 1] : static_cast<int>(nd - 1);
+  return static_cast<int>(nd - 1);
+}
+
+__device__ __forceinline__ int forced_token(const DevCfg& c, const RowMeta& rm, int V, float u, bool sample,
+                                            unsigned long long* kept) {
+  int zs[8];
+  const int nz = forced_zeros(c, rm, zs);
+  const unsigned long long cnt = nz ? static_cast<unsigned long long>(nz) : static_cast<unsigned long long>(V);
+  const int pos = equal_pick(c, cnt, u, sample, kept);
+  return nz ? zs[pos] : pos;
 }
 
 // Log-probability of a selected token (the log-softmax of the scores the
@@ -1804,6 +1835,27 @@ __device__ __forceinline__ RowSums block_row_sums(SelSmem& sm, unsigned long lon
   return r;
 }
 
+// A row's processor state breaks its layout (this thread's columns): an id
+// outside [-1, V), or within a processor's columns an unused (-1) column
+// before a used one, or used ids not strictly ascending.
+__device__ __forceinline__ bool state_layout_bad(const DevCfg& c, const int32_t* ids) {
+  const int S = c.pcol[c.nproc];
+  bool bad = false;
+  for (int j = threadIdx.x; j < S; j += kThreads) {
+    int end = S;
+    for (int k = 0; k < c.nproc; ++k)
+      if (j < c.pcol[k + 1]) { end = c.pcol[k + 1]; break; }
+    const int t = __ldg(ids + j);
+    if (t < -1 || t >= c.V) {
+      bad = true;
+    } else if (j + 1 < end) {
+      const int t2 = __ldg(ids + j + 1);
+      if (t == -1 ? t2 != -1 : (t2 != -1 && t2 <= t)) bad = true;
+    }
+  }
+  return bad;
+}
+
 // VMODE: 0 select, 1 verify, 2 verify with the processors at every position
 // (a compile-time choice, so plain verify carries none of the bitmap code).
 template <int DT, int VMODE, bool SAMPLE>
@@ -1827,8 +1879,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   const bool tempered = SAMPLE && c.temp != 1.0f;
   // rows take the TMA ring when every row starts on a 16-byte boundary
   const bool tma_ok = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0u) && ((static_cast<size_t>(V) * esz) % 16u == 0u);
-  const bool bitmaps = (!VERIFY || VHIST) && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
-                                   (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
+  // rows with the task's processors: their state ids are marked and listed;
+  // a row that cannot finish on the one-pass path is left to state_kernel
+  const bool state = !VERIFY && a.st_ids != nullptr;
+  const int S = state ? c.pcol[c.nproc] : 0;
+  const bool bitmaps = (!VERIFY || VHIST) && (state || c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 ||
+                                               c.n_seq > 0 || (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
 
   // Inputs may come from the kernel before this one in the stream.
   grid_dependency_wait();
@@ -1860,6 +1916,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         if (!VERIFY && SAMPLE && a.logprobs) a.logprobs[myrow] = __int_as_float(0x7fc00000);   // no token: NaN
         if (rm.bad) atomicOr(c.status, kFlagBadRow);
         if (VERIFY) verify_ticket(c, a, myrow);
+      } else if (rm.forced && state) {
+        a.out[myrow] = kDeferred;
       } else if (rm.forced) {
         const float u = (SAMPLE && a.uniforms) ? a.uniforms[myrow] : 0.0f;
         unsigned long long kept = 1ull;
@@ -1926,11 +1984,28 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     if (tid == 0) sm.misc.dbg_row = row;
 #endif
     TG_T(row, 0);
+    // the row's processor state: its layout is checked first (a row whose
+    // state breaks it is deferred, and state_kernel flags and drops it)
+    const int32_t* sids = nullptr;
+    const float* svals = nullptr;
+    bool defer = false;
+    if (state) {
+      sids = a.st_ids + static_cast<size_t>(row) * S;
+      svals = a.st_vals + static_cast<size_t>(row) * S;
+      if (tid < kStateFilterWords) sm.misc.sfilt[tid] = 0u;
+      csync();
+      for (int j = tid; j < S; j += kThreads) {
+        const int t = __ldg(sids + j);
+        if (t >= 0) atomicOr(&sm.misc.sfilt[(t >> 5) & (kStateFilterWords - 1)], 1u << (t & 31));
+      }
+      defer = __syncthreads_or(state_layout_bad(c, sids) ? 1 : 0) != 0;
+    }
     // the candidate list is free at the start of a row: it stages the history
     // the marked tokens are listed too (in N's words) when they fit
     const int nlist = bitmaps ? build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s),
-                                                  2 * kCandCap, &sm.misc.lctr)
+                                                  2 * kCandCap, &sm.misc.lctr, sids, S)
                               : -1;
+    if (state && nlist < 0) defer = true;
     TG_T(row, 1);
 
     float bv = -INFINITY;            // greedy: this lane's best unmarked score and index
@@ -2040,7 +2115,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         if (s > bv || (s == bv && static_cast<unsigned>(t) < bi)) { bv = s; bi = static_cast<unsigned>(t); }
       };
       if (bitmaps && nlist >= 0) {
-        for_listed<DT>(N, nlist, rowp, [&](float x, int t, bool banned, int) { merge(process_marked(c, x, banned, false), t); });
+        for_listed<DT>(N, nlist, rowp, [&](float x, int t, unsigned e, int) {
+          merge(process_listed(c, x, e, sids, svals, sm.misc.sfilt, false), t);
+        });
       } else if (bitmaps) {
         for_marked<DT>(sm, rowp, M, a.nwords, [&](float x, int t) { merge(process_elem(c, M, N, x, t, false), t); });
       }
@@ -2100,8 +2177,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         };
         if (bitmaps && nlist >= 0) {
           // listed: each processed score replaces its entry; the weights follow once m is known
-          for_listed<DT>(N, nlist, rowp, [&](float x, int t, bool banned, int j) {
-            const float s = process_marked(c, x, banned, true);
+          for_listed<DT>(N, nlist, rowp, [&](float x, int t, unsigned e, int j) {
+            const float s = process_listed(c, x, e, sids, svals, sm.misc.sfilt, true);
             mk_max = fmaxf(mk_max, s);
             push(s, t);
             N[j] = __float_as_uint(s);
@@ -2151,7 +2228,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
           // directly (the row is likely still in L2), with a lower threshold.
           // (a draw without top_p that misses its target lies in the bulk of the
           // row; only the exact path helps there)
-          if (slow && reason == 5) {
+          if (slow && reason == 5 && !state) {
             TG_T(row, 5);
             const FinResult fr2 = second_chance<DT>(c, a, sm, rm, rowp, M, N, bitmaps, theta_raw - 2.0f * T, tempered, m,
                                                     static_cast<unsigned long long>(Zsigned), u, topk, topp);
@@ -2165,7 +2242,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       }
       TG_DBG(row, 0, slow ? 1 : 0); TG_DBG(row, 1, reason);
       TG_T(row, 6);
-      if (slow) {
+      if (slow && state) {
+        defer = true;
+      } else if (slow) {
         const SlowPick sp = slow_select<DT>(c, a, sm, rm, rowp, M, N, bitmaps, u);
         tok = sp.token;
         tok_score = sp.score;
@@ -2179,8 +2258,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     // ---------------- outputs ----------------
     TG_T(row, 7);
     if (tid == 0) {
-      a.out[row] = token;
-      if (SAMPLE && !VERIFY && a.logprobs) a.logprobs[row] = token_logprob(tok_score, tok_ref, tok_fast, tok_S);
+      // a row deferred here takes state_kernel's exact path: counted as slow
+      if (defer) { atomicOr(c.status, kFlagSlow); atomicAdd(c.slow_rows, 1ull); }
+      a.out[row] = defer ? kDeferred : token;
+      if (SAMPLE && !VERIFY && a.logprobs && !defer) a.logprobs[row] = token_logprob(tok_score, tok_ref, tok_fast, tok_S);
       if (VERIFY) verify_ticket(c, a, row);
     }
     csync();
@@ -2221,36 +2302,37 @@ struct ProcSmem {
 // needs no processing), and fill the per-row fields of cr.  A state that breaks its layout is
 // dropped for the row and raises kFlagBadState.  P has nwords words.
 __device__ __forceinline__ void state_row_setup(DevCfg& cr, const RowMeta& rm, const int32_t* st_ids,
-                                                const float* st_vals, int row, unsigned* P, int nwords) {
+                                                const float* st_vals, int row, unsigned* P, int nwords,
+                                                int* stage_ids, float* stage_vals) {
   const int S = cr.pcol[cr.nproc];
   const int32_t* ids = st_ids + static_cast<size_t>(row) * S;
+  const float* vals = st_vals + static_cast<size_t>(row) * S;
   for (int w = threadIdx.x; w < nwords; w += kThreads) P[w] = 0u;
   __syncthreads();
-  bool bad = false;
+  // the state is staged in shared memory: the processors search it per token
   for (int j = threadIdx.x; j < S; j += kThreads) {
-    int end = S;
-    for (int k = 0; k < cr.nproc; ++k)
-      if (j < cr.pcol[k + 1]) { end = cr.pcol[k + 1]; break; }
     const int t = __ldg(ids + j);
-    if (t < -1 || t >= cr.V) {
-      bad = true;
-    } else if (j + 1 < end) {
-      const int t2 = __ldg(ids + j + 1);
-      if (t == -1 ? t2 != -1 : (t2 != -1 && t2 <= t)) bad = true;
-    }
+    stage_ids[j] = t;
+    stage_vals[j] = __ldg(vals + j);
     if (t >= 0 && t < cr.V) set_bit(P, t);
   }
-  bad = __syncthreads_or(bad) != 0;
+  const bool bad = __syncthreads_or(state_layout_bad(cr, ids) ? 1 : 0) != 0;
   if (bad && threadIdx.x == 0) atomicOr(cr.status, kFlagBadState);
   cr.prow = true;
   cr.forced_row = rm.forced;
   cr.nfz = rm.forced ? forced_zeros(cr, rm, cr.fz) : 0;
   if (threadIdx.x < cr.nfz) set_bit(P, cr.fz[threadIdx.x]);
   __syncthreads();
-  cr.pst_ids = bad ? nullptr : ids;
-  cr.pst_vals = bad ? nullptr : st_vals + static_cast<size_t>(row) * S;
+  cr.pst_ids = bad ? nullptr : stage_ids;
+  cr.pst_vals = bad ? nullptr : stage_vals;
   cr.pbits = P;
 }
+
+// Shared memory after the row bitmaps' area in state_kernel (where select_kernel
+// keeps its TMA ring): the state bitmap P, the staged state (S ids, S values),
+// and a forced row's list of tokens above F (S + 8 scores and ids).
+__host__ __device__ constexpr int state_stage_bytes(int S) { return align_up(8 * S, 128); }
+__host__ __device__ constexpr int sparse_list_bytes(int S) { return align_up(8 * (S + 8), 128); }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -2271,8 +2353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   DevCfg cr = c;
   if (st_ids != nullptr) {
-    unsigned* P = reinterpret_cast<unsigned*>(smem_raw + fixed + 2 * bitmap_bytes(a.nwords));
-    state_row_setup(cr, rm, st_ids, st_vals, row, P, a.nwords);
+    unsigned char* area = smem_raw + fixed + 2 * bitmap_bytes(a.nwords);
+    unsigned* P = reinterpret_cast<unsigned*>(area);
+    int* sid = reinterpret_cast<int*>(area + bitmap_bytes(a.nwords));
+    const int S = c.pcol[c.nproc];
+    state_row_setup(cr, rm, st_ids, st_vals, row, P, a.nwords, sid, reinterpret_cast<float*>(sid + S));
   }
   const void* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * (DT == kF32 ? 4 : 2);
   float* sc = out_scores + static_cast<size_t>(row) * V;
@@ -2355,15 +2440,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // ---------------------------------------------------------------------------
-// state_kernel: tg_select_state, the selection with the task's processors
+// state_kernel: the rows of tg_select_state that select_kernel deferred
+// (out == kDeferred): forced rows, rows whose marked tokens do not fit the
+// list, rows that need the exact path, rows whose state breaks its layout
 // (Transmuter.Generation, section "Processors").  One CTA per row at a time
-// (grid-stride over the rows).  Per row: the state is checked and its ids set
-// in a bitmap P (in the space the TMA ring takes in select_kernel), the row
-// bitmaps are built, and every token is processed by process_elem, which
-// takes the processor path (forced rows included).  Greedy: one pass, block
-// argmax (lowest index on ties).  Sampling: the exact multi-pass selection
-// of select_kernel's slow path (row maximum, fixed-point mass, top_k / top_p
-// cut and draw by value windows or radix selection), uncounted.
+// (grid-stride over the rows).  Per row: the state is checked and its ids
+// (and a forced row's forced ids) set in a bitmap P, in the space the TMA
+// ring takes in select_kernel; the row bitmaps are built; every token is
+// processed by process_elem, which takes the processor path.  Greedy: one
+// pass and a block argmax (lowest index on ties).  Sampling: the exact
+// multi-pass selection of select_kernel's slow path, uncounted.  A forced row
+// scores F except at its P tokens, which are all the passes visit (F tokens
+// weigh nothing); when none scores above F every token ties.
 // ---------------------------------------------------------------------------
 template <int DT, bool SAMPLE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -2372,11 +2460,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   unsigned* H = reinterpret_cast<unsigned*>(smem_raw + fin_offset());
   unsigned* N = H + bitmap_bytes(a.nwords) / 4;
-  unsigned* P = reinterpret_cast<unsigned*>(smem_raw + ring_offset(a.nwords));
+  unsigned char* area = smem_raw + ring_offset(a.nwords);
+  unsigned* P = reinterpret_cast<unsigned*>(area);
+  const int S = c.pcol[c.nproc];
+  int* stage_ids = reinterpret_cast<int*>(area + bitmap_bytes(a.nwords));
+  float* stage_vals = reinterpret_cast<float*>(stage_ids + S);
+  float* sp_s = reinterpret_cast<float*>(area + bitmap_bytes(a.nwords) + state_stage_bytes(S));
+  unsigned* sp_i = reinterpret_cast<unsigned*>(sp_s + S + 8);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int V = a.V;
   constexpr int esz = DT == kF32 ? 4 : 2;
   for (int row = blockIdx.x; row < a.nrows; row += gridDim.x) {
+    if (a.fixup && __ldcg(a.out + row) != kDeferred) continue;
+#ifdef TG_DEBUG
+    if (tid == 0) sm.misc.dbg_row = row;
+#endif
+    TG_T(row, 0);
     const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
     if (rm.bad || rm.L == 0) {
       if (tid == 0) {
@@ -2387,11 +2486,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       continue;
     }
     DevCfg cr = c;
-    state_row_setup(cr, rm, st_ids, st_vals, row, P, a.nwords);
-    build_row_bitmaps(cr, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+    state_row_setup(cr, rm, st_ids, st_vals, row, P, a.nwords, stage_ids, stage_vals);
+    TG_T(row, 1);
+    // a forced row scores F, 0 or a processor's value: it needs no row bitmaps
+    if (!rm.forced) build_row_bitmaps(cr, a.hist, rm, H, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+    TG_T(row, 2);
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
-    if (!SAMPLE) {
-      RowGlobalSource<DT> src{rowp, V, &cr, H, N, true, false};
+    const float u = (SAMPLE && a.uniforms) ? a.uniforms[row] : 0.0f;
+    unsigned long long live = 1ull;
+    if (rm.forced) {
+      // list the tokens above F once (forced ids and state ids; final scores)
+      if (tid == 0) sm.misc.ncand = 0;
+      __syncthreads();
+      for (int w = tid; w < a.nwords; w += kThreads) {
+        unsigned bits = P[w];
+        while (bits) {
+          const int i = w * 32 + __ffs(bits) - 1;
+          bits &= bits - 1u;
+          float sc = process_state_elem(cr, H, N, 0.0f, i);
+          if (SAMPLE && cr.temp != 1.0f) sc = clampf(__fdiv_rn(sc, cr.temp));
+          if (sc > kFilter) {
+            const int pos = atomicAdd(&sm.misc.ncand, 1);
+            sp_s[pos] = sc;
+            sp_i[pos] = static_cast<unsigned>(i);
+          }
+        }
+      }
+      __syncthreads();
+      cr.sparse_row = true;
+      cr.sp_s = sp_s;
+      cr.sp_i = sp_i;
+      cr.sp_n = sm.misc.ncand;
+      live = static_cast<unsigned long long>(cr.sp_n);
+      // top_k at or above the tokens above F keeps all of them (the rest weigh nothing)
+      if (live > 0ull && static_cast<unsigned long long>(cr.top_k) >= live) cr.top_k = 0;
+    }
+    TG_T(row, 3);
+    if (live == 0ull) {
+      // every token scores F: all V tie
+      if (tid == 0) {
+        unsigned long long kept = 1ull;
+        a.out[row] = equal_pick(cr, static_cast<unsigned long long>(V), u, SAMPLE, &kept);
+        if (SAMPLE && a.logprobs) a.logprobs[row] = -logf(static_cast<float>(kept));
+      }
+    } else if (!SAMPLE) {
+      RowGlobalSource<DT> src{rowp, V, &cr, H, N, !rm.forced, false};
       src.state_row(cr);
       float bv = -INFINITY;
       unsigned bi = 0xffffffffu;
@@ -2417,13 +2556,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.out[row] = static_cast<int>(b);
       }
     } else {
-      const float u = a.uniforms ? a.uniforms[row] : 0.0f;
-      const SlowPick sp = slow_select<DT>(cr, a, sm, rm, rowp, H, N, true, u, false);
-      if (tid == 0) {
-        a.out[row] = static_cast<int>(sp.token);
-        if (a.logprobs) a.logprobs[row] = token_logprob(sp.score, sp.ref, sp.fast, sp.S);
+      bool done = false;
+      if (rm.forced && cr.sp_n <= kCandCap) {
+        // the one-pass path's candidate finish: the listed tokens hold all of
+        // the row's mass (the rest score F and weigh nothing)
+        const int n = cr.sp_n;
+        float mx = -INFINITY, mn = INFINITY;
+        for (int j = tid; j < n; j += kThreads) {
+          sm.cand_s[j] = sp_s[j];
+          sm.cand_i[j] = sp_i[j];
+          mx = fmaxf(mx, sp_s[j]);
+          mn = fminf(mn, sp_s[j]);
+        }
+        const float m = block_max(mx, &sm.red);
+        const float lo = -block_max(-mn, &sm.red);
+        const float cc = m * kLog2e;
+        unsigned long long z = 0ull;
+        for (int j = tid; j < n; j += kThreads) z += wfix_fast(sp_s[j], cc);
+        const unsigned long long Z = block_sum_u64(z, &sm.red);
+        if (tid == 0) sm.misc.ncand = n;
+        csync();
+        const bool topk = cr.top_k > 0 && cr.top_k < V;
+        const bool topp = cr.top_p < 1.0f;
+        const FinResult fr = finalize2(cr, sm, m, lo, Z, u, topk, topp);
+        if (fr.ok) {
+          if (tid == 0) {
+            a.out[row] = static_cast<int>(fr.token);
+            if (a.logprobs) a.logprobs[row] = token_logprob(fr.score, cc, true, fr.S);
+          }
+          done = true;
+        }
+      }
+      if (!done) {
+        const SlowPick sp = slow_select<DT>(cr, a, sm, rm, rowp, H, N, !rm.forced, u, false);
+        if (tid == 0) {
+          a.out[row] = static_cast<int>(sp.token);
+          if (a.logprobs) a.logprobs[row] = token_logprob(sp.score, sp.ref, sp.fast, sp.S);
+        }
       }
     }
+    TG_T(row, 4);
     __syncthreads();
   }
 }
@@ -2554,11 +2726,13 @@ extern "C" tg_status tg_verify_noalloc(const void* target_logits, int32_t B, int
 namespace tg {
 
 int select_smem_bytes(int nstage, int nwords) { return ring_offset(nwords) + nstage * kStageBytes; }
-int process_smem_bytes(int nwords) {
-  // the row bitmaps and the state bitmap
-  return align_up(static_cast<int>(sizeof(ProcSmem)), 128) + 3 * bitmap_bytes(nwords);
+int process_smem_bytes(int nwords, int S) {
+  // the row bitmaps, the state bitmap and the staged state
+  return align_up(static_cast<int>(sizeof(ProcSmem)), 128) + 3 * bitmap_bytes(nwords) + state_stage_bytes(S);
 }
-int state_smem_bytes(int nwords) { return ring_offset(nwords) + bitmap_bytes(nwords); }
+int state_smem_bytes(int nwords, int S) {
+  return ring_offset(nwords) + bitmap_bytes(nwords) + state_stage_bytes(S) + sparse_list_bytes(S);
+}
 
 // One launch per kMaxRowsPerCta * grid rows; each is a programmatic dependent
 // of the kernel before it in the stream (its launch overlaps that kernel's

@@ -252,3 +252,34 @@ def test_benchmark_rows_with_processors():
     ids2, lps2, _ = gpu_select_state(w)
     ids3, lps3, _ = gpu_select_state(w)
     assert np.array_equal(ids2, ids3) and np.array_equal(lps2.view(np.uint32), lps3.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_rows_left_to_the_exact_path(mode):
+    """Rows select_kernel hands to state_kernel: histories too long to stage
+    (9,000 ids), forced rows under top_k (more and fewer tokens above the
+    filter value than k), and a draw without top_p (the exact path)."""
+    V = 5000
+    rng = np.random.default_rng(12)
+    hists = [rng.integers(0, V, 9000).astype(np.int32), rng.integers(0, V, 20).astype(np.int32),
+             np.arange(3, dtype=np.int32), np.arange(3, dtype=np.int32), rng.integers(0, V, 40).astype(np.int32)]
+    plens = [100, 5, 1, 1, 40]
+    ids, off = W._pack(hists)
+    logits = rng.normal(0, 2, (len(hists), V)).astype(np.float32)
+    params = dict(vocab=V, logits_dtype="f32", mode=mode, top_k=2, top_p=1.0, repetition_penalty=1.3,
+                  no_repeat_ngram_size=2, forced_eos_token_ids=[2, 8], max_new_tokens=3,
+                  processors=(("bias", 4), ("set", 3)))
+    w = W.Workload("deferred", params, logits, ids, off, np.array(plens, np.int32),
+                   rng.random(len(hists), dtype=np.float32))
+    st_ids = np.array([[int(hists[0][0]), 4000, -1, -1, 7, 9, -1],
+                       [-1, -1, -1, -1, int(hists[1][3]), -1, -1],
+                       [2, -1, -1, -1, 11, 12, 13],       # forced: 2, 8 and three set tokens above F
+                       [8, -1, -1, -1, -1, -1, -1],       # forced: only 2 and 8
+                       [5, 6, -1, -1, 5, -1, -1]], np.int32)
+    st_vals = np.array([[1.0, 2.0, 0, 0, 3.5, -1.0, 0],
+                        [0, 0, 0, 0, 6.0, 0, 0],
+                        [0.5, 0, 0, 0, 0.25, 1.0, -0.5],
+                        [-0.75, 0, 0, 0, 0, 0, 0],
+                        [0.5, 0.5, 0, 0, -2.0, 0, 0]], np.float32)
+    w.extra["state"] = (st_ids, st_vals)
+    compare_state(w, max_boundary_frac=1.0)
