@@ -304,11 +304,13 @@ tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, con
  * The processors run on the scores after the processors of tg_select (also
  * on a forced row, whose other tokens hold the filter value) and before
  * temperature, top_k, top_p and the draw.  A row whose state breaks its
- * layout runs without the processors and raises TG_FLAG_BAD_STATE.  One
- * thread block per row reads the row from global memory in several passes
- * (the multi-pass exact selection of tg_select); it does not count rows as
- * slow.  Other arguments, layouts and errors as tg_select; a cfg without
- * processors, or a NULL state pointer, is TG_ERR_INVALID_ARGUMENT.
+ * layout runs without the processors and raises TG_FLAG_BAD_STATE.  The
+ * state ids join the one-pass path of tg_select as marked tokens; a row that
+ * path cannot finish goes to a second kernel in the same stream (multi-pass,
+ * counted in the slow-row count).  out_ids may hold -2 between the two
+ * kernels, never after the call's work completes.  Other arguments, layouts
+ * and errors as tg_select; a cfg without processors, or a NULL state
+ * pointer, is TG_ERR_INVALID_ARGUMENT.
  */
 tg_status tg_select_state(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
                           const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,

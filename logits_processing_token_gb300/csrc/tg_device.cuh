@@ -566,19 +566,25 @@ static __device__ __noinline__ int build_row_bitmaps(const DevCfg& c, const int3
 // its state columns (ascending, -1 padding after them) by binary search; an
 // entry (t, v) makes s + v ("bias", one f32 add) or v ("set"), never below
 // the filter value.  The state may be in global or shared memory.
+// Column of t among one processor's n columns (ids in use ascending, -1
+// padding after them), or -1.
+__device__ __forceinline__ int state_find(const int* ids, int n, int t) {
+  int lo = 0, hi = n;   // first column whose id is unused (-1) or >= t
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int v = ids[mid];
+    if (v != -1 && v < t) lo = mid + 1; else hi = mid;
+  }
+  return (lo < n && ids[lo] == t) ? lo : -1;
+}
+
 __device__ __forceinline__ float apply_state_at(const DevCfg& c, const int* sids, const float* svals, float s,
                                                 int t) {
   for (int k = 0; k < c.nproc; ++k) {
-    const int c0 = c.pcol[k], n = c.pcol[k + 1] - c0;
-    const int* ids = sids + c0;
-    int lo = 0, hi = n;   // first column whose id is unused (-1) or >= t
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      const int v = ids[mid];
-      if (v != -1 && v < t) lo = mid + 1; else hi = mid;
-    }
-    if (lo < n && ids[lo] == t) {
-      const float v = svals[c0 + lo];
+    const int c0 = c.pcol[k];
+    const int j = state_find(sids + c0, c.pcol[k + 1] - c0, t);
+    if (j >= 0) {
+      const float v = svals[c0 + j];
       s = clampf(c.pkind[k] == 0 ? __fadd_rn(s, v) : v);
     }
   }

@@ -138,6 +138,7 @@ struct Misc {
   unsigned wu[kWarps];
   unsigned lvl[kWarps][4];               // first sub-chunk: packed counts per level of 2 below m0
   unsigned sfilt[kStateFilterWords];     // the row's state ids, as a 1,024-bit filter
+  int nfst;                              // forced rows with a state of this CTA (after the streamed ones)
 };
 
 constexpr int kLevels = 1024;   // value levels between the lowest candidate and the row max
@@ -1856,6 +1857,119 @@ __device__ __forceinline__ bool state_layout_bad(const DevCfg& c, const int32_t*
   return bad;
 }
 
+// A forced row with a processor state, block-wide: its tokens score F except
+// the forced ids (0) and the state ids (a processor's value), so the tokens
+// above F are listed once (a state id in its first processor's columns, a
+// forced id that is no state id) with their final scores, and the one-pass
+// finish selects from them (they hold all of the row's mass).  Every token at
+// F: all V tie.  Left at kDeferred for state_kernel when the list overflows
+// or the finish cannot decide.
+template <bool SAMPLE>
+__device__ __noinline__ void forced_state_row(const DevCfg& c, const SelArgs& a, SelSmem& sm, int row, int S) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int V = a.V;
+  const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
+  int zs[8];
+  const int nz = forced_zeros(c, rm, zs);
+  const int32_t* ids = a.st_ids + static_cast<size_t>(row) * S;
+  const float* vals = a.st_vals + static_cast<size_t>(row) * S;
+  csync();
+  const bool bad = __syncthreads_or(state_layout_bad(c, ids) ? 1 : 0) != 0;
+  if (tid == 0) {
+    if (bad) atomicOr(c.status, kFlagBadState);
+    sm.misc.ncand = 0;
+  }
+  csync();
+  for (int j = tid; j < S + nz; j += kThreads) {
+    int t;
+    bool dup = false;
+    if (j < S) {
+      t = bad ? -1 : __ldg(ids + j);
+      if (t < 0) continue;
+      for (int k = 0; k < c.nproc && c.pcol[k + 1] <= j; ++k)
+        dup = dup || state_find(ids + c.pcol[k], c.pcol[k + 1] - c.pcol[k], t) >= 0;
+    } else {
+      t = zs[j - S];
+      for (int k = 0; !bad && k < c.nproc; ++k)
+        dup = dup || state_find(ids + c.pcol[k], c.pcol[k + 1] - c.pcol[k], t) >= 0;
+    }
+    if (dup) continue;
+    float s = kFilter;
+    for (int q = 0; q < nz; ++q) s = zs[q] == t ? 0.0f : s;
+    if (!bad) s = apply_state_at(c, ids, vals, s, t);
+    if (SAMPLE && c.temp != 1.0f) s = clampf(__fdiv_rn(s, c.temp));
+    if (s > kFilter) {
+      const int pos = atomicAdd(&sm.misc.ncand, 1);
+      if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = static_cast<unsigned>(t); }
+    }
+  }
+  csync();
+  const int n = sm.misc.ncand;
+  if (n > kCandCap) return;
+  const float u = (SAMPLE && a.uniforms) ? a.uniforms[row] : 0.0f;
+  if (n == 0) {
+    if (tid == 0) {
+      unsigned long long kept = 1ull;
+      a.out[row] = equal_pick(c, static_cast<unsigned long long>(V), u, SAMPLE, &kept);
+      if (SAMPLE && a.logprobs) a.logprobs[row] = -logf(static_cast<float>(kept));
+    }
+    csync();
+    return;
+  }
+  if (!SAMPLE) {
+    float bv = -INFINITY;
+    unsigned bi = 0xffffffffu;
+    for (int j = tid; j < n; j += kThreads) {
+      const float v = sm.cand_s[j];
+      const unsigned i = sm.cand_i[j];
+      if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const unsigned i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (v2 > bv || (v2 == bv && i2 < bi)) { bv = v2; bi = i2; }
+    }
+    if (lane == 0) { sm.misc.wf[wid] = bv; sm.misc.wu[wid] = bi; }
+    csync();
+    if (tid == 0) {
+      float v = sm.misc.wf[0];
+      unsigned b = sm.misc.wu[0];
+      for (int q = 1; q < kWarps; ++q) {
+        const float v2 = sm.misc.wf[q];
+        const unsigned i2 = sm.misc.wu[q];
+        if (v2 > v || (v2 == v && i2 < b)) { v = v2; b = i2; }
+      }
+      a.out[row] = static_cast<int>(b);
+    }
+    csync();
+    return;
+  }
+  float mx = -INFINITY, mn = INFINITY;
+  for (int j = tid; j < n; j += kThreads) {
+    mx = fmaxf(mx, sm.cand_s[j]);
+    mn = fminf(mn, sm.cand_s[j]);
+  }
+  const float m = block_max(mx, &sm.red);
+  const float lo = -block_max(-mn, &sm.red);
+  const float cc = m * kLog2e;
+  unsigned long long z = 0ull;
+  for (int j = tid; j < n; j += kThreads) z += wfix_fast(sm.cand_s[j], cc);
+  const unsigned long long Z = block_sum_u64(z, &sm.red);
+  // top_k at or above the tokens above F keeps all of them (the rest weigh nothing)
+  const bool topk = c.top_k > 0 && c.top_k < n;
+  const FinResult fr = finalize2(c, sm, m, lo, Z, u, topk, c.top_p < 1.0f);
+  if (tid == 0) {
+    if (fr.ok) {
+      a.out[row] = static_cast<int>(fr.token);
+      if (a.logprobs) a.logprobs[row] = token_logprob(fr.score, cc, true, fr.S);
+    } else {
+      atomicOr(c.status, kFlagSlow);
+      atomicAdd(c.slow_rows, 1ull);
+    }
+  }
+  csync();
+}
+
 // VMODE: 0 select, 1 verify, 2 verify with the processors at every position
 // (a compile-time choice, so plain verify carries none of the bitmap code).
 template <int DT, int VMODE, bool SAMPLE>
@@ -1904,6 +2018,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   const int rel = a.nrows - a.row_begin - static_cast<int>(blockIdx.x);
   const int nmine = rel > 0 ? min(kMaxRowsPerCta, (rel - 1) / static_cast<int>(gridDim.x) + 1) : 0;
   bool streamed = false;
+  bool fstate = false;   // a forced row with a processor state: finished after the streamed rows
   int myrow = 0;
   if (tid < nmine) {
     myrow = a.row_begin + static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x);
@@ -1917,7 +2032,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
         if (rm.bad) atomicOr(c.status, kFlagBadRow);
         if (VERIFY) verify_ticket(c, a, myrow);
       } else if (rm.forced && state) {
-        a.out[myrow] = kDeferred;
+        a.out[myrow] = kDeferred;   // until this CTA finishes it (or state_kernel does)
+        fstate = true;
       } else if (rm.forced) {
         const float u = (SAMPLE && a.uniforms) ? a.uniforms[myrow] : 0.0f;
         unsigned long long kept = 1ull;
@@ -1944,6 +2060,21 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     if (streamed) sm.rows[before + __popc(bal & ((1u << lane) - 1u))] = myrow;
     if (tid == 0) sm.misc.nrow = total;
     __syncthreads();
+    if (state) {
+      // then the forced rows with a state, after them
+      const unsigned bal2 = __ballot_sync(0xffffffffu, fstate);
+      if (lane == 0) sm.misc.wu[wid] = static_cast<unsigned>(__popc(bal2));
+      __syncthreads();
+      int before2 = 0, total2 = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        const int cq = static_cast<int>(sm.misc.wu[q]);
+        before2 += q < wid ? cq : 0;
+        total2 += cq;
+      }
+      if (fstate) sm.rows[total + before2 + __popc(bal2 & ((1u << lane) - 1u))] = myrow;
+      if (tid == 0) sm.misc.nfst = total2;
+      __syncthreads();
+    }
   }
   const int nrow = sm.misc.nrow;
   const int total_seq = nrow * nsub;   // <= kMaxRowsPerCta * (TG_MAX_VOCAB * 4 / kStageBytes)
@@ -2275,6 +2406,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       const int n = sm.misc.iss[s];
       if (n > 0) mbar_wait(&sm.misc.full[s], static_cast<unsigned>((n - 1) & 1));
     }
+  }
+  // forced rows with a state, block-wide (the row bitmaps' area is free now);
+  // after an error they stay deferred to state_kernel
+  if (state && !sm.misc.error) {
+    const int nf = sm.misc.nfst;
+    for (int q = 0; q < nf; ++q) forced_state_row<SAMPLE>(c, a, sm, sm.rows[nrow + q], S);
   }
 }
 
