@@ -32,7 +32,7 @@ What it computes, step by step, in the order the pages give:
   adjust the candidate count (+2 if all match, -1 otherwise, 5 at first).
 
 The pages name the processors but do not print their formulas.  The readings
-taken here (each listed in the design doc) are:
+taken here are:
 
 * repetition_penalty: each distinct id of the history in [0, V) takes
   x * rho if its ORIGINAL logit x < 0, else x / rho.
@@ -45,6 +45,9 @@ taken here (each listed in the design doc) are:
   rounding leaves none, the last kept token.
 * greedy skips temperature/top_k/top_p and takes the lowest index among the
   maximal scores.
+* the task's processors leave their function open; here "bias" (s + v) and
+  "set" (v) over a sparse per-row state of (id, value) entries, in list
+  order, never below the filter value.
 
 Elementwise arithmetic is IEEE fp32 one operation at a time (numpy float32
 scalars/arrays, no fused multiply-add).  Softmax masses and cumulative sums
