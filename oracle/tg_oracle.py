@@ -49,6 +49,11 @@ taken here are:
   "set" (v) over a sparse per-row state of (id, value) entries, in list
   order, never below the filter value.
 
+Each function is pinned by tests/test_oracle_pins.py to these readings
+(closed forms, worked rules of the pages, brute force, exact rationals).
+Their equivalence with the transformers processors that the names refer to
+is parity unpinned: that library is not available to test against.
+
 Elementwise arithmetic is IEEE fp32 one operation at a time (numpy float32
 scalars/arrays, no fused multiply-add).  Softmax masses and cumulative sums
 are fp64.  Everything here is a straight loop or a library primitive (sort,
