@@ -283,3 +283,20 @@ def test_rows_left_to_the_exact_path(mode):
                         [0.5, 0.5, 0, 0, -2.0, 0, 0]], np.float32)
     w.extra["state"] = (st_ids, st_vals)
     compare_state(w, max_boundary_frac=1.0)
+
+
+def test_largest_workload_sampled_rows():
+    """B=1,024, V=262,144 f32 Student-t rows (histories up to 4,096 Zipf ids,
+    repetition penalty, 4-gram bans, top_p 0.9) with a bias of 48 and a set
+    of 16 columns per row: every 32nd row against the oracle."""
+    w = with_state(W.config5(), procs=(("bias", 48), ("set", 16)), seed=8)
+    rows = list(range(0, w.B, 32))
+    _, _, _, n = compare_state(w, rows=rows)
+    assert n >= 28
+
+
+def test_benchmark_rows_greedy_with_processors():
+    w = W.config3(B=64)
+    w.params["mode"] = "greedy"
+    with_state(w, procs=(("set", 16), ("bias", 16)), seed=6)
+    compare_state(w)
