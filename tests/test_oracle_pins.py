@@ -801,3 +801,66 @@ def test_invalid_processor_state_is_dropped():
         s, _, info = O.process_row(x, [1], 1, p, st)
         assert info.bad_state and np.array_equal(s, x)
     assert O.processor_state_valid(np.array([0, 9, -1], np.int32), p)
+
+
+def _full_bias(V, c):
+    """A state that lists every token once in one bias processor, each with value c."""
+    return np.arange(V, dtype=np.int32), np.full(V, c, np.float32)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_uniform_bias_changes_no_selection(mode):
+    """Softmax, argmax, top_k, top_p and the draw are invariant under a shift of
+    every score by one constant: a bias of c on every token (dyadic values, so
+    the f32 adds are exact) must leave ids and log-probabilities unchanged.  A
+    bias placed after temperature, or applied to a subset, breaks this."""
+    rng = np.random.default_rng(31)
+    V = 24
+    for trial in range(40):
+        x = (rng.integers(-24, 24, V) * 0.25).astype(np.float32)
+        h = [int(t) for t in rng.integers(0, V, 6)]
+        kw = dict(vocab=V, mode=mode, temperature=0.5, top_k=int(rng.integers(0, 6)),
+                  top_p=float(rng.choice([1.0, 0.7])), repetition_penalty=2.0)
+        u = float(rng.random())
+        t0, i0 = O.select_row(x, h, 2, P(**kw), u)
+        t1, i1 = O.select_row(x, h, 2, P(processors=(("bias", V),), **kw), u, _full_bias(V, 3.0))
+        assert t1 == t0, trial
+        assert abs(i1.logprob - i0.logprob) < 1e-9, trial
+
+
+def test_bias_zero_and_set_to_current_score_are_identities():
+    V = 10
+    x = np.array([1.5, -2.0, 0.25, 3.0, -0.5, 0.0, 2.5, -1.25, 0.75, 1.0], np.float32)
+    h = [3, 3, 6]
+    base, banned0, _ = O.process_row(x, h, 1, P(vocab=V, repetition_penalty=1.5, suppress_tokens=[1]))
+    s1, banned1, _ = O.process_row(x, h, 1, P(vocab=V, repetition_penalty=1.5, suppress_tokens=[1],
+                                             processors=(("bias", V),)), _full_bias(V, 0.0))
+    ids = np.arange(V, dtype=np.int32)
+    s2, _, _ = O.process_row(x, h, 1, P(vocab=V, repetition_penalty=1.5, suppress_tokens=[1],
+                                       processors=(("set", V),)), (ids, base.copy()))
+    assert np.array_equal(s1.view(np.uint32), base.view(np.uint32))
+    assert np.array_equal(s2.view(np.uint32), base.view(np.uint32))
+    assert np.array_equal(banned1, banned0)
+
+
+def test_two_biases_compose_and_a_huge_negative_bias_removes_a_token():
+    V = 8
+    x = np.array([0.5, 2.0, -1.0, 1.75, 0.0, -0.25, 1.0, 3.0], np.float32)
+    # two processors biasing the same token add up (dyadic values: exact)
+    two = (np.array([7, 7], np.int32), np.array([-1.5, -0.75], np.float32))
+    s2, _, _ = O.process_row(x, [0], 1, P(vocab=V, processors=(("bias", 1), ("bias", 1))), two)
+    one = (np.array([7], np.int32), np.array([-2.25], np.float32))
+    s1, _, _ = O.process_row(x, [0], 1, P(vocab=V, processors=(("bias", 1),)), one)
+    assert np.array_equal(s1, s2) and s1[7] == np.float32(0.75)
+    # a bias of -FLT_MAX takes a finite score to the filter value (the f32 add rounds there)
+    to_f = (np.array([7], np.int32), np.array([F], np.float32))
+    s, _, _ = O.process_row(x, [0], 1, P(vocab=V, processors=(("bias", 1),)), to_f)
+    assert s[7] == F
+    # a bias of -3e38 leaves the token finite but without mass: never selected, as if suppressed
+    far = (np.array([7], np.int32), np.array([-3e38], np.float32))
+    s, _, _ = O.process_row(x, [0], 1, P(vocab=V, processors=(("bias", 1),)), far)
+    assert s[7] == np.float32(-3e38) and s[7] > F
+    for u in np.linspace(0.0, 0.999, 41):
+        t, _ = O.select_row(x, [0], 1, P(vocab=V, mode="sample", processors=(("bias", 1),)), float(u), far)
+        t_sup, _ = O.select_row(x, [0], 1, P(vocab=V, mode="sample", suppress_tokens=[7]), float(u))
+        assert t == t_sup and t != 7
