@@ -38,6 +38,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph-captured timing")
     ap.add_argument("--beam", action="store_true",
                     help="time tg_beam_step (64 prompts x 4 beams over the same rows) instead of tg_select")
     ap.add_argument("--state", action="store_true",
@@ -185,6 +186,44 @@ def required_bytes(w):
         if L > 0 and not forced:
             n_read += 1
     return n_read * w.V * elt + hist + w.B * 20 + 8, n_read
+
+
+def graph_timing(launch, rows, steps):
+    """The same step launched from a CUDA graph: `launch(i)` issues step i on
+    the current stream; up to 20 consecutive steps (rotating over the logits
+    copies) are captured once and the graph is replayed until about `steps`
+    steps ran.  Any failure to capture or replay is reported, not raised."""
+    import torch
+    try:
+        n_cap = max(1, min(20, steps))
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(2):
+                launch(i)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for i in range(n_cap):
+                launch(i)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // n_cap)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * n_cap)
+        return {"value": whole_job_rate(1, rows, ms), "unit": "rows/s", "ms_per_step": ms,
+                "steps_per_graph": n_cap, "replays": reps}
+    except Exception as e:  # reported in the line instead of ending the run
+        return {"unavailable": "%s: %s" % (type(e).__name__, str(e)[:200])}
 
 
 def cpu_baseline(w, seconds):
@@ -350,6 +389,11 @@ def run_ours(args):
         e_ms = max_over_ranks(e_ms, world, "cuda")
         line["e2e"] = {"value": whole_job_rate(world, B, e_ms), "unit": "rows/s", "h2d_bytes_per_step": bi,
                        "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
+
+    if not args.no_graph and world == 1:
+        # (at N = 1 only: a rank whose capture failed would leave the others in the max-over-ranks collective)
+        line["graph"] = graph_timing(
+            lambda i: tg.tg_select(sets[i % n_sets], hid, off, pl, cfg, u, out, out_logprobs=lp), B, K)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

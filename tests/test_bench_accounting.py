@@ -30,3 +30,13 @@ def test_required_bytes_of_the_benchmark_step():
     # 32 of the 256 rows are forced-eos rows (b % 8 == 1): 224 rows read 151,936 bf16 logits each
     assert n_read == 224
     assert got == 224 * 151_936 * 2 + 4 * int(w.hist_offsets[-1]) + 256 * 20 + 8 == 68_867_928
+
+
+def test_graph_timing_reports_a_failure_instead_of_raising():
+    # without a usable GPU the capture cannot start: the line gets the reason
+    import torch
+    if torch.cuda.is_available():
+        import pytest
+        pytest.skip("a GPU is present: the failure path is not reachable this way")
+    got = bench.graph_timing(lambda i: None, 256, 10)
+    assert set(got) == {"unavailable"} and got["unavailable"]
