@@ -864,3 +864,29 @@ def test_two_biases_compose_and_a_huge_negative_bias_removes_a_token():
         t, _ = O.select_row(x, [0], 1, P(vocab=V, mode="sample", processors=(("bias", 1),)), float(u), far)
         t_sup, _ = O.select_row(x, [0], 1, P(vocab=V, mode="sample", suppress_tokens=[7]), float(u))
         assert t == t_sup and t != 7
+
+
+def test_final_distribution_closed_forms():
+    """The distribution the draw uses: the kept set renormalised, 0 elsewhere.
+    Weights 4:2:1:1 under top_p 0.7 keep the first two (0.75 >= 0.7): 2/3, 1/3;
+    top_k 2 over scores (1, 1, 1, 0) keeps all three tied tokens: 1/3 each."""
+    V = 4
+    s = np.array([np.log(4.0), np.log(2.0), 0.0, 0.0], np.float32)
+    d = O.final_distribution(s, P(vocab=V, mode="sample", top_p=0.7))
+    assert np.allclose(d, [2 / 3, 1 / 3, 0.0, 0.0], rtol=0, atol=1e-7)
+    d = O.final_distribution(np.array([1.0, 1.0, 1.0, 0.0], np.float32), P(vocab=V, mode="sample", top_k=2))
+    assert np.allclose(d, [1 / 3, 1 / 3, 1 / 3, 0.0], rtol=0, atol=1e-12)
+    # no warper: the plain softmax, summing to one
+    x = np.array([0.5, -1.0, 2.0, 0.0], np.float32)
+    d = O.final_distribution(x, P(vocab=V, mode="sample"))
+    e = np.exp(x.astype(np.float64))
+    assert np.allclose(d, e / e.sum(), rtol=1e-12) and abs(d.sum() - 1.0) < 1e-12
+
+
+def test_log_softmax_at_closed_forms():
+    # weights 1 : 3 -> log(3/4) at the larger; filter-value tokens add nothing
+    s = np.array([0.0, np.log(3.0), F, F], np.float32)
+    assert abs(O.log_softmax_at(s, 1) - math.log(0.75)) < 1e-7
+    assert abs(O.log_softmax_at(s, 0) - math.log(0.25)) < 1e-7
+    # every token at the filter value: uniform over V
+    assert abs(O.log_softmax_at(np.full(5, F, np.float32), 3) + math.log(5.0)) < 1e-12
