@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtg.so")
 SOURCES = ["tg_kernels.cu", "tg_api.cu", "tg_beam.cu"]
-HEADERS = ["tg_device.cuh", os.path.join("..", "..", "include", "tg.h")]
+HEADERS = ["tg_device.cuh", "tg_select_core.cuh", os.path.join("..", "..", "include", "tg.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

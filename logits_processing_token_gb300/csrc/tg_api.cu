@@ -479,6 +479,8 @@ tg_status tg_clear_status(const tg_config* cfg) {
   if (st != TG_OK) return st;
   cudaError_t e = cudaMemset(cfg->dev.status, 0, sizeof(unsigned));
   if (e == cudaSuccess) e = cudaMemset(cfg->dev.slow_rows, 0, sizeof(unsigned long long));
+  // tickets a launch left behind (one whose bounded wait ran out) start at zero again
+  if (e == cudaSuccess) e = cudaMemset(cfg->dev.tickets, 0, static_cast<size_t>(cfg->max_batch) * sizeof(unsigned));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return from_cuda(e);
 }
