@@ -59,6 +59,11 @@ typedef enum { TG_GREEDY = 0, TG_SAMPLE = 1 } tg_mode;
 #define TG_FLAG_HISTORY_ID_OUT_OF_RANGE 0x1u /* a history id was < 0 or >= V; skipped */
 #define TG_FLAG_BAD_ROW 0x2u                 /* offsets/prompt length inconsistent; row gave -1 */
 #define TG_FLAG_SLOW_PATH 0x4u               /* a row needed the multi-pass exact path */
+/* A bounded wait on a bulk copy ran out (about 1 s): the launch stopped
+ * loading logits.  The rows it had not finished give -1 in out_ids /
+ * out_next (log-probability NaN); in verify, their batch rows give
+ * out_match = -1.  Every other output of the call is valid. */
+#define TG_FLAG_TIMEOUT 0x8u
 #define TG_FLAG_BAD_STATE 0x10u              /* a row's processor state broke its layout; dropped */
 
 /* Largest vocabulary the kernels take. */
@@ -218,6 +223,10 @@ tg_status tg_select_logprobs(const void* logits, int32_t B, int32_t V, const int
  *
  * Position j selects with cfg's mode and warpers (temperature, top_k,
  * top_p); history processors do not run per position.  B <= cfg's max_batch.
+ * A batch row whose positions a timed-out launch left unfinished gives
+ * out_match = -1 (TG_FLAG_TIMEOUT).  Calls on one config share its per-row
+ * counts of finished positions (cleared on `stream` at the start of each
+ * call): run them in stream order.
  */
 tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids,
                     int32_t K, const tg_config* cfg, const float* uniforms, int32_t* out_match,
@@ -238,6 +247,16 @@ tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hi
                      const int64_t* hist_offsets, const int32_t* prompt_lens,
                      const tg_config* cfg, float* out_scores, uint32_t* out_banbits,
                      float* out_probs, tg_stream stream);
+
+/*
+ * tg_set_wait_limit -- testing.  The select and verify kernels give up a
+ * wait on a bulk copy of logits after about one second (TG_FLAG_TIMEOUT);
+ * this sets that limit to `cycles` SM cycles on the current device, for the
+ * launches that follow (0 restores the default).  The wait for copies still
+ * in flight after such an error keeps the full limit, so no copy outlives
+ * its CTA.  Not for use while other calls run.  Errors: TG_ERR_CUDA.
+ */
+tg_status tg_set_wait_limit(uint64_t cycles);
 
 /* Largest B that tg_verify_noalloc takes. */
 #define TG_NOALLOC_MAX_BATCH 1024
@@ -260,7 +279,8 @@ tg_status tg_process(const void* logits, int32_t B, int32_t V, const int32_t* hi
  * TG_ERR_UNSUPPORTED when B > TG_NOALLOC_MAX_BATCH or V > TG_MAX_VOCAB;
  * TG_ERR_INVALID_ARGUMENT for a bad setting or pointer; TG_ERR_CUDA when the
  * set-up or the launch fails.  Device-side status bits of this entry point
- * are not reported.
+ * are not reported; a batch row that a timed-out launch left unfinished
+ * gives out_match = -1 (and -1 in its unfinished out_next entries).
  *
  * The first call on a device does a one-time synchronous set-up on the
  * current device (it resolves the array's address and zeroes it); make that

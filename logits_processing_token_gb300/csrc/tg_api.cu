@@ -332,6 +332,10 @@ tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32
   a.out_match = out_match;
   a.nstage = cfg->ver.nstage;
   a.nwords = 0;
+  // this call's counts of finished positions start at zero
+  cudaError_t e = cudaMemsetAsync(cfg->dev.tickets, 0, static_cast<size_t>(B) * sizeof(unsigned),
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e);
   int grid = std::min<long long>(a.nrows, static_cast<long long>(cfg->ver.blocks_per_sm) * cfg->nsm);
   return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->ver.smem, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -366,6 +370,10 @@ tg_status tg_verify_history(const void* target_logits, int32_t B, int32_t V, con
   // the row bitmaps need the select kernel's shared-memory plan
   a.nstage = cfg->sel.nstage;
   a.nwords = cfg->nwords;
+  // this call's counts of finished positions start at zero
+  cudaError_t e = cudaMemsetAsync(cfg->dev.tickets, 0, static_cast<size_t>(B) * sizeof(unsigned),
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e);
   int grid = std::min<long long>(a.nrows, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm);
   return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
   }
   grid_dependents_launch();
 
+  if (tid == 0) sm.misc.nrow_done = nrow;
   int cur_st = 0;          // stage and phase of the next sub-chunk of the schedule
   unsigned cur_ph = 0u;
   for (int ri = 0; ri < nrow; ++ri) {
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       if (lane == 0) { sm.misc.wf[wid] = bv; sm.misc.wu[wid] = bi; }
       if (tid == 0) sm.misc.err_snap = *reinterpret_cast<volatile int*>(&sm.misc.error);
       csync();
-      if (sm.misc.err_snap) break;   // uniform: every thread reads the same snapshot
+      if (sm.misc.err_snap) { if (tid == 0) sm.misc.nrow_done = ri; break; }   // uniform snapshot
       if (tid == 0) {
         float v = sm.misc.wf[0];
         unsigned b = sm.misc.wu[0];
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
       }
       csync();
       TG_T(row, 15);
-      if (sm.misc.err_snap) break;
+      if (sm.misc.err_snap) { if (tid == 0) sm.misc.nrow_done = ri; break; }
       float m_raw = -INFINITY;
       for (int q = 0; q < kWarps; ++q) m_raw = fmaxf(m_raw, sm.misc.wf[q]);
       bool slow = !decided || !tma_ok || !(m_raw > kFilter);
@@ -580,13 +581,24 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
     csync();
   }
 
-  // error: wait (bounded) for the copies still in flight, then leave
+  // error: wait (bounded) for the copies still in flight, then leave.  No
+  // copy is issued once the error flag is set, and an issued bulk copy
+  // completes unless the memory system itself fails.  The rows this CTA did
+  // not finish get -1 (verify: their batch row's out_match too; its count of
+  // finished positions never completes, so no other CTA writes it).
   __syncthreads();
   if (sm.misc.error && tid == 0) {
     atomicOr(c.status, kFlagTimeout);
     for (int s = 0; s < nst; ++s) {
       const int n = sm.misc.iss[s];
-      if (n > 0) mbar_wait(&sm.misc.full[s], static_cast<unsigned>((n - 1) & 1));
+      if (n > 0) mbar_drain(&sm.misc.full[s], static_cast<unsigned>((n - 1) & 1));
+    }
+  }
+  if (sm.misc.error) {
+    for (int q = sm.misc.nrow_done + tid; q < nrow; q += kThreads) {
+      const int row = sm.rows[q];
+      a.out[row] = -1;
+      if (VERIFY) a.out_match[row / (a.K + 1)] = -1;
     }
   }
   // forced rows with a state, block-wide (the row bitmaps' area is free now);
@@ -1152,6 +1164,13 @@ cudaError_t select_occupancy(int dtype, bool verify, int smem, int* blocks_per_s
   }
   *blocks_per_sm = worst;
   return cudaSuccess;
+}
+
+// Testing: the select kernels' streaming waits give up after `cycles` SM
+// cycles (0: the default, about one second).
+extern "C" tg_status tg_set_wait_limit(uint64_t cycles) {
+  const unsigned long long v = cycles ? static_cast<unsigned long long>(cycles) : kWaitLimitCycles;
+  return cudaMemcpyToSymbol(g_wait_limit, &v, sizeof(v)) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
 #ifdef TG_DEBUG

@@ -79,14 +79,29 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned 
       : "memory");
   return ok != 0u;
 }
-// Bounded wait: false after ~1 s without completion.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (static_cast<unsigned long long>(clock64() - t0) > kWaitLimitCycles) return false;
+// Limit of the streaming waits in SM cycles (kWaitLimitCycles, ~1 s; a
+// test may shorten it to make the waits run out).
+__device__ unsigned long long g_wait_limit = kWaitLimitCycles;
+
+// Bounded wait: false when the phase did not complete within `limit`
+// cycles.  (try_wait may itself suspend the thread until the phase completes,
+// so a completion seen later than the limit counts as a timeout too.)
+__device__ __forceinline__ bool mbar_wait_for(unsigned long long* bar, unsigned parity, unsigned long long limit) {
+  const long long t0 = clock64();
+  for (;;) {
+    const bool done = mbar_try_wait(bar, parity);
+    const unsigned long long dt = static_cast<unsigned long long>(clock64() - t0);
+    if (done) return dt <= limit;
+    if (dt > limit) return false;
   }
-  return true;
+}
+// A streaming wait (g_wait_limit).
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
+  return mbar_wait_for(bar, parity, *static_cast<volatile unsigned long long*>(&g_wait_limit));
+}
+// The wait for copies still in flight after an error: always the full ~1 s.
+__device__ __forceinline__ bool mbar_drain(unsigned long long* bar, unsigned parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitCycles);
 }
 
 // ---------------------------------------------------------------------------
@@ -114,6 +129,7 @@ struct Misc {
   unsigned lvl[kWarps][4];               // first sub-chunk: packed counts per level of 2 below m0
   unsigned sfilt[kStateFilterWords];     // the row's state ids, as a 1,024-bit filter
   int nfst;                              // forced rows with a state of this CTA (after the streamed ones)
+  int nrow_done;                         // after a timeout: the first streamed row left unfinished
 };
 
 constexpr int kLevels = 2 * kThreads;   // value levels between the lowest candidate and the row max

@@ -25,6 +25,7 @@ TG_GREEDY, TG_SAMPLE = 0, 1
 TG_FLAG_HISTORY_ID_OUT_OF_RANGE = 0x1
 TG_FLAG_BAD_ROW = 0x2
 TG_FLAG_SLOW_PATH = 0x4
+TG_FLAG_TIMEOUT = 0x8
 TG_FLAG_BAD_STATE = 0x10
 TG_MAX_VOCAB = 1 << 18
 TG_PROC_BIAS, TG_PROC_SET = 0, 1
@@ -35,7 +36,7 @@ TG_MAX_STATE_COLS = 4096
 EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
            "tg_status_string", "tg_verify_noalloc", "tg_beam_step", "tg_beam_keep",
-           "tg_verify_history", "tg_select_state", "tg_process_state")
+           "tg_verify_history", "tg_select_state", "tg_process_state", "tg_set_wait_limit")
 TG_NOALLOC_MAX_BATCH = 1024
 
 
@@ -112,6 +113,8 @@ def load_library(path: str | None = None):
     lib.tg_verify_noalloc.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_int32, POINTER(tg_params), c_void_p,
                                       c_void_p, c_void_p, c_void_p]
     lib.tg_verify_noalloc.restype = c_int
+    lib.tg_set_wait_limit.argtypes = [c_uint64]
+    lib.tg_set_wait_limit.restype = c_int
     lib.tg_process.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_void_p, c_void_p]
     lib.tg_select_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -474,6 +477,13 @@ def tg_query_status(cfg: Config):
 
 def tg_clear_status(cfg: Config):
     _check("tg_clear_status", load_library().tg_clear_status(cfg.handle))
+
+
+def tg_set_wait_limit(cycles: int):
+    """Testing: the select/verify kernels give up a bulk-copy wait after
+    ``cycles`` SM cycles (0 restores the default of about one second)."""
+    lib = load_library()
+    _check("tg_set_wait_limit", lib.tg_set_wait_limit(int(cycles)))
 
 
 def tg_next_num_candidates(K: int, n_match: int, K_max: int) -> int:

@@ -164,3 +164,18 @@ def test_binding_checks_the_state_shape():
         tg.tg_select_state(*args, torch.zeros(2, 4, dtype=i32), torch.zeros(2, 5), None, torch.zeros(2, dtype=i32))
     with pytest.raises(ValueError, match="state_values"):
         tg.tg_process_state(*args, torch.zeros(2, 5, dtype=i32), torch.zeros(2, 4), torch.zeros(2, 64))
+
+
+def test_status_flags_agree_across_header_binding_and_kernels():
+    # every status bit the kernels raise is declared in include/tg.h, with the
+    # same value in the binding
+    import re
+    from logits_processing_token_gb300 import tg as T
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = open(os.path.join(root, "include", "tg.h")).read()
+    declared = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define TG_FLAG_(\w+) (0x[0-9a-fA-F]+)u", hdr)}
+    dev = open(os.path.join(root, "logits_processing_token_gb300", "csrc", "tg_device.cuh")).read()
+    raised = {int(m.group(1), 16) for m in re.finditer(r"constexpr unsigned kFlag\w+ = (0x[0-9a-fA-F]+)u", dev)}
+    assert raised == set(declared.values())
+    for name, value in declared.items():
+        assert getattr(T, "TG_FLAG_" + name) == value
