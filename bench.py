@@ -34,11 +34,12 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph-captured timing")
+    ap.add_argument("--quick", action="store_true", help="the headline workload only (no other configurations)")
     ap.add_argument("--beam", action="store_true",
                     help="time tg_beam_step (64 prompts x 4 beams over the same rows) instead of tg_select")
     ap.add_argument("--state", action="store_true",
@@ -226,8 +227,8 @@ def graph_timing(launch, rows, steps):
         return {"unavailable": "%s: %s" % (type(e).__name__, str(e)[:200])}
 
 
-def cpu_baseline(w, seconds):
-    """The oracle as it stands, timed on host cores over a bounded sample of rows."""
+def cpu_baseline_1core(w, seconds):
+    """The oracle as it stands, on one host core, over a bounded sample of rows."""
     from oracle import tg_oracle as O
     p = O.Params(**w.params)
     t0 = time.perf_counter()
@@ -241,23 +242,221 @@ def cpu_baseline(w, seconds):
         if el >= seconds or n >= 4 * w.B:
             break
     return {"value": n / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": "%d rows of the same workload (row-by-row numpy oracle, one thread), %.1f s" % (n, el)}
+            "sample": "%d rows of the same workload (row-by-row numpy oracle, one process), %.1f s" % (n, el)}
+
+
+_OW = None
+
+
+def _oracle_init(shm_name, shape, dtype, hist_ids, hist_offsets, prompt_lens, params, uniforms):
+    global _OW
+    import numpy as np
+    from multiprocessing import shared_memory
+    from oracle import tg_oracle as O
+    shm = shared_memory.SharedMemory(name=shm_name)
+    logits = np.ndarray(shape, dtype=np.dtype(dtype), buffer=shm.buf)
+    _OW = (shm, logits, hist_ids, hist_offsets, prompt_lens, O.Params(**params), uniforms)
+
+
+def _oracle_rows(rows):
+    from oracle import tg_oracle as O
+    _, logits, hid, off, pl, p, u = _OW
+    ids, infos = O.select(logits, hid, off, pl, p, u, rows=rows)
+    return [(int(r), int(i), bool(f.u_boundary or f.topp_boundary)) for r, i, f in zip(rows, ids, infos)]
+
+
+class OraclePool:
+    """The oracle as it stands on every host core the process may use: one
+    spawned worker per core, the logits shared (not copied) between them."""
+
+    def __init__(self, w):
+        import multiprocessing as mp
+        import numpy as np
+        from multiprocessing import shared_memory
+        self.cores = len(os.sched_getaffinity(0))
+        self.shm = shared_memory.SharedMemory(create=True, size=w.logits.nbytes)
+        np.ndarray(w.logits.shape, dtype=w.logits.dtype, buffer=self.shm.buf)[:] = w.logits
+        self.pool = mp.get_context("spawn").Pool(
+            self.cores, initializer=_oracle_init,
+            initargs=(self.shm.name, w.logits.shape, w.logits.dtype.str, w.hist_ids, w.hist_offsets, w.prompt_lens,
+                      w.params, w.uniforms))
+        self.pool.map_async(_oracle_rows, [[] for _ in range(self.cores)]).get(timeout=300)   # workers up first
+
+    def run(self, rows):
+        """(seconds, [(row, id, on_boundary)]) for the listed rows."""
+        rows = list(rows)
+        parts = [rows[i::self.cores] for i in range(self.cores)]
+        t0 = time.perf_counter()
+        res = self.pool.map_async(_oracle_rows, parts).get(timeout=600)
+        el = time.perf_counter() - t0
+        return el, sorted(x for part in res for x in part)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self.shm.close()
+        self.shm.unlink()
+
+
+def oracle_check(w, gpu_ids, pool=None):
+    """The oracle on all cores over every row of w: its rate, the rows whose
+    uniform or top-p cut lies within 1e-6 of a boundary, and how many of the
+    GPU's ids equal the oracle's (all rows, and off the boundaries)."""
+    own = pool is None
+    pool = pool or OraclePool(w)
+    try:
+        el, res = pool.run(range(w.B))
+    finally:
+        if own:
+            pool.close()
+    boundary = sum(1 for _, _, bnd in res if bnd)
+    equal = sum(1 for r, i, _ in res if int(gpu_ids[r]) == i)
+    equal_off = sum(1 for r, i, bnd in res if not bnd and int(gpu_ids[r]) == i)
+    return {"value": w.B / el, "unit": "rows/s", "cores": pool.cores, "kind": "oracle",
+            "sample": "all %d rows of the workload, one spawned process per core, %.2f s" % (w.B, el),
+            "seconds": el, "boundary_rows": boundary, "ids_equal": equal, "ids_equal_off_boundary": equal_off,
+            "rows_off_boundary": w.B - boundary}
+
+
+def time_select(w, steps, warmup, gpu_index, clocks=True, logprobs=False):
+    """tg_select on workload w, inputs resident in HBM (rotating over enough
+    copies of the logits to exceed L2): stream and CUDA-graph timings, the
+    roofline of the launch, and the ids of the last step."""
+    import numpy as np
+    import torch
+    import logits_processing_token_gb300 as tg
+    bf16 = w.params["logits_dtype"] == "bf16"
+    cfg = tg.Config(**w.params)
+    elt = 2 if bf16 else 4
+    nbytes = w.B * w.V * elt
+    n_sets = max(1, int(np.ceil(2.5 * L2_BYTES / nbytes)))
+    host = torch.from_numpy(w.logits.view(np.int16) if bf16 else w.logits)
+    sets = [host.cuda().view(torch.bfloat16) if bf16 else host.cuda() for _ in range(n_sets)]
+    hid = torch.from_numpy(w.hist_ids).cuda()
+    off = torch.from_numpy(w.hist_offsets).cuda()
+    pl = torch.from_numpy(w.prompt_lens).cuda()
+    u = torch.from_numpy(w.uniforms).cuda()
+    out = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    lp = torch.empty(w.B, dtype=torch.float32, device="cuda") if logprobs else None
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        tg.tg_select(sets[i % n_sets], hid, off, pl, cfg, u, out, stream=stream, out_logprobs=lp)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    tg.tg_clear_status(cfg)
+    ck = Clocks(gpu_index, enabled=clocks)
+    ck.start()
+    time.sleep(0.3 if ck.proc else 0.0)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = ck.stop()
+    ms = e0.elapsed_time(e1) / steps
+    flags, slow_rows = tg.tg_query_status(cfg)
+    ids = out.cpu().numpy()
+    graph = graph_timing(lambda i: tg.tg_select(sets[i % n_sets], hid, off, pl, cfg, u, out, out_logprobs=lp), w.B,
+                         steps)
+    peak, peak_kind = measured_peak()
+    alg, n_read = required_bytes(w)
+    achieved = alg / (ms / 1000.0) / 1e9
+    res = {"workload": w.name, "B": w.B, "V": w.V, "logits_dtype": w.params["logits_dtype"],
+           "us_per_step": ms * 1000.0, "rows_per_s": w.B / (ms / 1000.0),
+           "logits_gbs": nbytes / (ms / 1000.0) / 1e9,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                        "peak_source": "%s hbm_gbs (copy)" % peak_kind, "bytes_per_launch": alg,
+                        "rows_reading_logits": n_read, "traffic": None},
+           "graph": graph, "slow_path_rows": slow_rows, "status_flags": flags, "steps": steps, "warmup": warmup,
+           "l2": "inputs rotate over %d copies of the logits (%.0f MB)" % (n_sets, n_sets * nbytes / 1e6)}
+    if clk:
+        res["clocks"] = clk
+    del sets
+    torch.cuda.empty_cache()
+    return res, ids
+
+
+def time_verify(B, K, mode, steps, warmup):
+    """tg_verify on config 4's inputs (candidates agree with the target's
+    argmax at the seeded positions): microseconds per call."""
+    import numpy as np
+    import torch
+    import logits_processing_token_gb300 as tg
+    from logits_processing_token_gb300 import workloads as W
+    w = W.config4(B=B, K=K, mode=mode)
+    tgt = torch.from_numpy(np.ascontiguousarray(w.extra["target"])).cuda()
+    greedy = tgt.argmax(dim=-1)[:, :K].cpu().numpy()
+    cand = torch.from_numpy(W.make_candidates(greedy, w.extra["agree"], w.extra["offsets"], w.V)).cuda()
+    cfg = tg.Config(**w.params, max_batch=max(64, B))
+    u = torch.from_numpy(np.ascontiguousarray(w.uniforms)).cuda()
+    om = torch.empty(B, dtype=torch.int32, device="cuda")
+    on = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+    for _ in range(warmup):
+        tg.tg_verify(tgt, cand, K, cfg, u, om, on)
+    torch.cuda.synchronize()
+    tg.tg_clear_status(cfg)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        tg.tg_verify(tgt, cand, K, cfg, u, om, on)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flags, slow_rows = tg.tg_query_status(cfg)
+    nbytes = B * (K + 1) * w.V * 4
+    peak, _ = measured_peak()
+    return {"B": B, "K": K, "mode": mode, "us_per_call": ms * 1000.0, "logits_gbs": nbytes / (ms / 1000.0) / 1e9,
+            "hbm_frac": nbytes / (ms / 1000.0) / 1e9 / peak, "slow_path_rows": slow_rows, "status_flags": flags,
+            "l2": "target logits %.0f MB, not rotated (smaller calls run from L2)" % (nbytes / 1e6)}
+
+
+def main_config(w, n_sets, logprobs=False):
+    """The config dict both arms print for the headline workload."""
+    return {"workload": WORKLOAD, "B": w.B, "V": w.V, "logits_dtype": "bf16", "rows_per_gpu": w.B,
+            "parallelism": "replicas (rows independent, no collective)",
+            "l2": "inputs rotate over %d copies of the logits (%.0f MB) > L2" % (n_sets, n_sets * w.B * w.V * 2 / 1e6),
+            "logprobs": bool(logprobs)}
+
+
+def headline_sets(w):
+    import numpy as np
+    return max(2, int(np.ceil(2.5 * L2_BYTES / (w.B * w.V * 2))))
 
 
 def run_reference(args):
+    """The oracle as it stands, on all host cores: each step selects a
+    rotating sample of the workload's rows (four per core)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     from logits_processing_token_gb300 import workloads as W
     w = W.config3()
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    base = cpu_baseline(w, per_step * args.steps)
-    val = base["value"]
+    pool = OraclePool(w)
+    per = min(w.B, 4 * pool.cores)
+    try:
+        def step(i):
+            start = (i * per) % w.B
+            return pool.run([(start + k) % w.B for k in range(per)])[0]
+        for i in range(args.warmup):
+            step(i)
+        total = sum(step(args.warmup + i) for i in range(args.steps))
+    finally:
+        pool.close()
+    ms = 1000.0 * total / args.steps
+    val = per / (ms / 1000.0)
     line = {"metric": METRIC, "value": val, "unit": "rows/s", "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.B / val,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "B": w.B, "V": w.V, "logits_dtype": "bf16"},
-            "cpu_baseline": base,
+            "data": "synthetic", "config": main_config(w, headline_sets(w), args.logprobs),
+            "cpu_baseline": {"value": val, "unit": "rows/s", "cores": pool.cores, "kind": "oracle",
+                             "sample": "each step: %d of the %d rows (rotating), one spawned process per core" %
+                                       (per, w.B)},
             "e2e": {"value": val, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -280,8 +479,7 @@ def run_ours(args):
     B, V = w.B, w.V
     cfg = tg.Config(**w.params)
     # Enough distinct copies of the logits that consecutive steps never hit L2.
-    row_bytes = B * V * 2
-    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / row_bytes)))
+    n_sets = headline_sets(w)
     host_logits = torch.from_numpy(w.logits.view(np.int16))
     sets = [host_logits.cuda().view(torch.bfloat16) for _ in range(n_sets)]
     hid = torch.from_numpy(w.hist_ids).cuda()
@@ -336,11 +534,7 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": B, "V": V, "logits_dtype": "bf16", "rows_per_gpu": B,
-                       "parallelism": "replicas (rows independent, no collective)",
-                       "l2": "inputs rotate over %d copies of the logits (%.0f MB) > L2" %
-                             (n_sets, n_sets * row_bytes / 1e6),
-                       "logprobs": bool(args.logprobs)},
+            "config": main_config(w, n_sets, args.logprobs),
             "logits_gbs": nominal_gbs, "logits_hbm_frac": nominal_gbs / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
@@ -351,52 +545,87 @@ def run_ours(args):
     if clk:
         line["clocks"] = clk
 
+    ids_main = out.cpu().numpy()
     if not args.no_e2e:
-        # the public API from host buffers: H2D of every input, the call, D2H of the ids
+        # The public API from host buffers: every step copies all of its inputs
+        # from pinned host memory and reads its ids back.  Step i+1's copies run
+        # on a second stream while step i's kernel runs (two sets of device
+        # buffers); the kernel of a step waits for its own copies.
         h_logits = host_logits.pin_memory()
-        h_hid = torch.from_numpy(w.hist_ids).pin_memory()
-        h_off = torch.from_numpy(w.hist_offsets).pin_memory()
-        h_pl = torch.from_numpy(w.prompt_lens).pin_memory()
-        h_u = torch.from_numpy(w.uniforms).pin_memory()
-        h_out = torch.empty(B, dtype=torch.int32).pin_memory()
-        h_lp = torch.empty(B, dtype=torch.float32).pin_memory() if lp is not None else None
-        d_logits = torch.empty_like(h_logits, device="cuda")
-        bi = sum(t.numel() * t.element_size() for t in (h_logits, h_hid, h_off, h_pl, h_u))
-        bo = h_out.numel() * 4 + (h_lp.numel() * 4 if h_lp is not None else 0)
-
-        def e2e_step():
-            d_logits.copy_(h_logits, non_blocking=True)
-            hid.copy_(h_hid, non_blocking=True)
-            off.copy_(h_off, non_blocking=True)
-            pl.copy_(h_pl, non_blocking=True)
-            u.copy_(h_u, non_blocking=True)
-            tg.tg_select(d_logits.view(torch.bfloat16), hid, off, pl, cfg, u, out, stream=stream, out_logprobs=lp)
-            h_out.copy_(out, non_blocking=True)
-            if lp is not None:
-                h_lp.copy_(lp, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
+        h_small = [torch.from_numpy(a).pin_memory() for a in (w.hist_ids, w.hist_offsets, w.prompt_lens, w.uniforms)]
+        h_out = torch.empty((2, B), dtype=torch.int32).pin_memory()
+        h_lp = torch.empty((2, B), dtype=torch.float32).pin_memory() if lp is not None else None
+        d_logits = [torch.empty_like(h_logits, device="cuda") for _ in range(2)]
+        d_small = [[torch.empty_like(t, device="cuda") for t in h_small] for _ in range(2)]
+        d_out = [torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(2)]
+        d_lp = [torch.empty(B, dtype=torch.float32, device="cuda") for _ in range(2)] if lp is not None else None
+        bi = h_logits.numel() * h_logits.element_size() + sum(t.numel() * t.element_size() for t in h_small)
+        bo = B * 4 + (B * 4 if lp is not None else 0)
+        copy_stream = torch.cuda.Stream()
+        copied = [torch.cuda.Event() for _ in range(2)]
+        used = [torch.cuda.Event() for _ in range(2)]
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+
+        def e2e_run(n):
+            e0.record(stream)
+            copy_stream.wait_event(e0)
+            for i in range(n):
+                b = i % 2
+                with torch.cuda.stream(copy_stream):
+                    if i >= 2:
+                        copy_stream.wait_event(used[b])
+                    d_logits[b].copy_(h_logits, non_blocking=True)
+                    for d, h in zip(d_small[b], h_small):
+                        d.copy_(h, non_blocking=True)
+                    copied[b].record(copy_stream)
+                stream.wait_event(copied[b])
+                hid_b, off_b, pl_b, u_b = d_small[b]
+                tg.tg_select(d_logits[b].view(torch.bfloat16), hid_b, off_b, pl_b, cfg, u_b, d_out[b], stream=stream,
+                             out_logprobs=d_lp[b] if d_lp is not None else None)
+                used[b].record(stream)
+                h_out[b].copy_(d_out[b], non_blocking=True)
+                if h_lp is not None:
+                    h_lp[b].copy_(d_lp[b], non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+
+        e2e_run(3)
+        e_ms = e2e_run(args.e2e_steps)
         e_ms = max_over_ranks(e_ms, world, "cuda")
         line["e2e"] = {"value": whole_job_rate(world, B, e_ms), "unit": "rows/s", "h2d_bytes_per_step": bi,
-                       "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
+                       "d2h_bytes_per_step": bo, "ms_per_step": e_ms,
+                       "overlap": "step i+1's host-to-device copies run on a second stream during step i's kernel"}
 
     if not args.no_graph and world == 1:
         # (at N = 1 only: a rank whose capture failed would leave the others in the max-over-ranks collective)
         line["graph"] = graph_timing(
             lambda i: tg.tg_select(sets[i % n_sets], hid, off, pl, cfg, u, out, out_logprobs=lp), B, K)
 
+    if world == 1 and not args.quick:
+        # the other configurations, each timed the same way (inputs resident, > L2)
+        del sets
+        torch.cuda.empty_cache()
+        others = {}
+        for name, wk, st in (("1", W.config1(), args.steps), ("2", W.config2(), args.steps)):
+            others[name], _ = time_select(wk, st, args.warmup, local, clocks=False, logprobs=args.logprobs)
+        others["4"] = [time_verify(b, k, m, args.steps, args.warmup)
+                       for b, k, m in ((1, 5, "greedy"), (8, 5, "sample"), (32, 16, "greedy"), (32, 16, "sample"))]
+        line["configs"] = others
+        # config 5: B=1,024, V=262,144 f32 -- the second roofline target
+        w5 = W.config5()
+        c5, ids5 = time_select(w5, args.steps, args.warmup, local, clocks=not args.no_clocks, logprobs=args.logprobs)
+        c5["gpu_launches"] = args.steps
+        if not args.no_cpu_baseline:
+            c5["oracle"] = oracle_check(w5, ids5)
+        line["config5"] = c5
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        base = oracle_check(w, ids_main)
+        base["single_core"] = cpu_baseline_1core(w, args.cpu_seconds)
+        line["cpu_baseline"] = base
+        line["boundary_rows"] = base["boundary_rows"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
