@@ -551,6 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const DevCfg c, con
             tok = fr2.token;
             tok_score = fr2.score;
             tok_S = fr2.S;
+          } else if (slow && reason == 7 && !topk && !topp && !state) {
+            // a draw over the whole distribution that lands below the
+            // candidates: the tail's histogram, then the one bin it falls in
+            TG_T(row, 9);
+            const FinResult fr3 = tail_pick<DT>(c, a, sm, rm, rowp, M, N, bitmaps, theta_f, m,
+                                                static_cast<unsigned long long>(Zsigned), u);
+            slow = !fr3.ok;
+            if (slow) reason = 40 + fr3.reason;
+            tok = fr3.token;
+            tok_score = fr3.score;
+            tok_S = fr3.S;
           }
         }
       }

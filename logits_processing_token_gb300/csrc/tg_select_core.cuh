@@ -130,6 +130,8 @@ struct Misc {
   unsigned sfilt[kStateFilterWords];     // the row's state ids, as a 1,024-bit filter
   int nfst;                              // forced rows with a state of this CTA (after the streamed ones)
   int nrow_done;                         // after a timeout: the first streamed row left unfinished
+  int tbin;                              // tail_pick: the bin of the draw
+  unsigned long long tbefore;            // tail_pick: the tail's mass before that bin
 };
 
 constexpr int kLevels = 2 * kThreads;   // value levels between the lowest candidate and the row max
@@ -1473,6 +1475,98 @@ __device__ __forceinline__ LevelPick list_pick(SelSmem& sm, int n, float hi, flo
 }
 
 // Items whose key (order-preserving score key) lies in [klo, khi).
+// A draw without top_k and top_p whose target lies past every candidate (the
+// candidates hold the tokens scoring theta_f or more).  The row's tail
+// (scores below theta_f) is read again from L2 into an exact histogram of
+// the tail's fixed-point mass over kLevels bins of [m - 32, theta_f) (a score
+// further below weighs less than 2^-44 of the maximum's weight and falls into
+// the last bin); one block scan finds the bin in which the running mass,
+// taken in (score desc, index asc) order after the candidates', passes the
+// draw target; a third read lists that bin's tokens, and list_pick walks
+// them in that order.  Every thread calls; the candidate list, sm.ev and the
+// row bitmaps' area are free (the bitmaps are rebuilt).  Not ok when the bin
+// holds more tokens than the candidate list.
+template <int DT>
+__device__ __noinline__ FinResult tail_pick(const DevCfg& c, const SelArgs& a, SelSmem& sm, const RowMeta& rm,
+                                           const unsigned char* rowp, unsigned* M, unsigned* N, bool bitmaps,
+                                           float theta_f, float m, unsigned long long Z, float u) {
+  FinResult res{false, 40, 0u};
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float cc = m * kLog2e;
+  // the candidates' exact mass, in the weights of the finish
+  const int n = min(sm.misc.ncand, kCandCap);
+  unsigned long long zc = 0ull;
+  for (int i = tid; i < n; i += kThreads) zc += wfix_fast(sm.cand_s[i], cc);
+  const unsigned long long Zc = block_sum_u64(zc, &sm.red);
+  const unsigned long long Td = draw_target(u, Z);
+  if (Td < Zc) { res.reason = 41; return res; }
+  const unsigned long long R = Td - Zc;   // the draw's target within the tail
+  TG_TF(19);
+  static_assert(kEvCap * 4 >= kLevels * 8, "tail histogram");
+  unsigned long long* hm = reinterpret_cast<unsigned long long*>(sm.ev);
+  for (int l = tid; l < kLevels; l += kThreads) hm[l] = 0ull;
+  if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
+  else csync();
+  const float hi = theta_f, lo = m - 32.0f;
+  const float scale = hi > lo ? static_cast<float>(kLevels) / (hi - lo) : 0.0f;
+  auto bin = [&](float s) { return min(max(static_cast<int>((hi - s) * scale), 0), kLevels - 1); };
+  RowGlobalSource<DT> src{rowp, a.V, &c, M, N, bitmaps, true};
+  src.pass([&](float s, unsigned) {
+    if (s < hi) atomicAdd(&hm[bin(s)], wfix_fast(s, cc));
+  });
+  csync();
+  TG_TF(20);
+  // bins 2t and 2t+1 per thread: the tail's mass before them, then the bin
+  // whose running mass first passes R
+  const int l0 = 2 * tid, l1 = l0 + 1;
+  const unsigned long long m0 = hm[l0], m1 = hm[l1];
+  unsigned long long im = m0 + m1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, im, o);
+    if (lane >= o) im += t;
+  }
+  if (lane == 31) sm.red.q[wid] = im;
+  if (tid == 0) sm.misc.tbin = -1;
+  csync();
+  unsigned long long bm = im - (m0 + m1);
+  for (int q = 0; q < wid; ++q) bm += sm.red.q[q];
+  if (bm <= R && bm + m0 + m1 > R) {
+    if (bm + m0 > R) { sm.misc.tbin = l0; sm.misc.tbefore = bm; }
+    else { sm.misc.tbin = l1; sm.misc.tbefore = bm + m0; }
+  }
+  csync();
+  const int bs = sm.misc.tbin;
+  const unsigned long long before = sm.misc.tbefore;
+  if (bs < 0) { res.reason = 42; return res; }
+  // that bin's tokens become the candidates
+  if (tid == 0) sm.misc.ncand = 0;
+  csync();
+  float smax = -INFINITY, smin = INFINITY;
+  src.pass([&](float s, unsigned t) {
+    if (s < hi && bin(s) == bs) {
+      const int pos = atomicAdd(&sm.misc.ncand, 1);
+      if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = t; }
+      smax = fmaxf(smax, s);
+      smin = fminf(smin, s);
+    }
+  });
+  const float bhi = block_max(smax, &sm.red);
+  const float blo = -block_max(-smin, &sm.red);
+  if (sm.misc.ncand > kCandCap) { res.reason = 43; return res; }   // (read after block_max's barriers)
+  const int nb = sm.misc.ncand;
+  TG_TF(21);
+  TG_DBG(sm.misc.dbg_row, 6, nb);
+  const LevelPick d = list_pick(sm, nb, bhi, blo, cc, R - before, true, Zc + before);
+  TG_TF(22);
+  if (!d.ok) { res.reason = 44; return res; }
+  res.ok = true;
+  res.token = d.idx;
+  res.score = key2f(d.key);
+  res.S = Z;
+  return res;
+}
+
 struct InWindow {
   unsigned klo, khi;
   __device__ __forceinline__ bool operator()(unsigned key, unsigned) const { return key >= klo && key < khi; }

@@ -42,7 +42,7 @@ def run_gpu(w, tgt, cand, K):
 
 
 @pytest.mark.parametrize("B", [1, 8, 32])
-@pytest.mark.parametrize("K", [1, 5, 16])
+@pytest.mark.parametrize("K", [1, 2, 5, 8, 16])
 @pytest.mark.parametrize("mode", ["greedy", "sample"])
 def test_verify_parity(B, K, mode):
     w, tgt, cand, p = make_case(B, K, mode)
@@ -100,7 +100,7 @@ def run_gpu_history(w, tgt, cand, K, hists, plens):
 
 
 @pytest.mark.parametrize("mode", ["greedy", "sample"])
-@pytest.mark.parametrize("K", [1, 5, 16])
+@pytest.mark.parametrize("K", [1, 2, 5, 8, 16])
 def test_verify_history_parity(mode, K):
     """Processors at every position with the candidates as history: repetition
     penalty, 3-gram bans, bad words of several tokens, min_new_tokens, forced
