@@ -40,6 +40,8 @@ def parse_args():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph-captured timing")
     ap.add_argument("--quick", action="store_true", help="the headline workload only (no other configurations)")
+    ap.add_argument("--config", type=int, choices=[3, 5], default=3,
+                    help="5: time config 5 (B=1,024, V=262,144 f32, top_p 0.9) as the line's workload instead")
     ap.add_argument("--beam", action="store_true",
                     help="time tg_beam_step (64 prompts x 4 beams over the same rows) instead of tg_select")
     ap.add_argument("--state", action="store_true",
@@ -755,10 +757,38 @@ def run_state(args):
     print(json.dumps(line), flush=True)
 
 
+def run_config5(args):
+    """Config 5 as the line's workload: B=1,024 rows of V=262,144 f32 logits."""
+    import torch
+    from logits_processing_token_gb300 import _build
+    _build.build()
+    from logits_processing_token_gb300 import workloads as W
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    w = W.config5()
+    res, ids = time_select(w, args.steps, args.warmup, local, clocks=not args.no_clocks, logprobs=args.logprobs)
+    ms = res["us_per_step"] / 1000.0
+    line = {"metric": "rows/s and logits GB/s (% of GB300 HBM peak) at B=1,024, V=262,144", "value": res["rows_per_s"],
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "tg_select: " + w.name + ", repetition penalty 1.3, 4-gram ban, min_new_tokens 8",
+                       "B": w.B, "V": w.V, "logits_dtype": "f32", "l2": res["l2"], "logprobs": bool(args.logprobs)},
+            "roofline": dict(res["roofline"], kernel="select_kernel<f32>", mean_launch_us=res["us_per_step"]),
+            "graph": res["graph"], "gpu_launches": args.steps, "slow_path_rows": res["slow_path_rows"],
+            "status_flags": res["status_flags"]}
+    if "clocks" in res:
+        line["clocks"] = res["clocks"]
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_check(w, ids)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.config == 5:
+        run_config5(args)
     elif args.beam:
         run_beam(args)
     elif args.state:
