@@ -145,14 +145,28 @@ void tg_params_init(tg_params* p, int32_t vocab);
 /*
  * Validate *params and build a config on the current device: sorted
  * constant ban lists (bad words and suppress tokens), begin-suppress list,
- * status word and verify tickets.  Synchronous.  Errors:
+ * status word and verify tickets.  The uploads are enqueued on `stream`
+ * (NULL: the default stream) and the call waits for that stream before it
+ * returns, so the config is ready for any later call.  Errors:
  * TG_ERR_INVALID_ARGUMENT (a field out of range), TG_ERR_UNSUPPORTED
  * (V > TG_MAX_VOCAB), TG_ERR_OUT_OF_MEMORY, TG_ERR_CUDA.
  */
-tg_status tg_config_create(const tg_params* params, tg_config** out);
+tg_status tg_config_create(const tg_params* params, tg_config** out, tg_stream stream);
 
 /* Free the config's device memory (synchronises the device first). */
 tg_status tg_config_destroy(tg_config* cfg);
+
+/*
+ * For include/tg_custom.cuh (a task processor compiled by the caller):
+ * tg_config_view copies the config's device settings (a tg::DevCfg of
+ * `size` bytes: TG_ERR_INVALID_ARGUMENT when the size differs) to *out;
+ * tg_config_selection returns the config, owned by cfg, that selects from
+ * scores that already went through every processor and the temperature:
+ * f32 rows, cfg's mode, top_k and top_p, nothing else.  Its launches report
+ * in cfg's status word.
+ */
+tg_status tg_config_view(const tg_config* cfg, void* out, size_t size);
+const tg_config* tg_config_selection(const tg_config* cfg);
 
 /*
  * tg_select -- process and select one token per row.
@@ -353,6 +367,8 @@ tg_status tg_process_state(const void* logits, int32_t B, int32_t V, const int32
  * the multi-pass exact path since the last clear. */
 tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_rows);
 tg_status tg_clear_status(const tg_config* cfg);
+/* The status bits alone (synchronously): tg_query_status without the count. */
+tg_status tg_status_word(const tg_config* cfg, uint32_t* flags);
 
 /* Assisted Generation, step 6: the next candidate count.  K + 2 when
  * n_match == K (all candidates matched), else K - 1; bounded to [1, K_max]. */

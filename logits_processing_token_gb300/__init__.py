@@ -8,5 +8,5 @@ from .tg import (  # noqa: F401
     TG_GREEDY, TG_MAX_PROCESSORS, TG_MAX_STATE_COLS, TG_MAX_VOCAB, TG_NOALLOC_MAX_BATCH, TG_OK, TG_PROC_BIAS,
     TG_PROC_SET, TG_SAMPLE, Config, TGError, load_library, make_params, tg_clear_status, tg_beam_keep, tg_beam_step,
     tg_next_num_candidates, tg_params, tg_process, tg_process_state, tg_query_status, tg_select, tg_select_state,
-    tg_set_wait_limit, tg_status_string, tg_verify, tg_verify_history,
+    tg_set_wait_limit, tg_status_string, tg_status_word, tg_verify, tg_verify_history,
 )

@@ -29,6 +29,10 @@ struct tg_config {
   int proc_smem = 0;
   int state_smem = 0;
   void* dmem = nullptr;
+  // the config that selects from scores a task processor compiled by the
+  // caller has already produced (include/tg_custom.cuh): f32, the same mode,
+  // top_k and top_p, every processor and the temperature off
+  tg_config* plain = nullptr;
 };
 
 namespace {
@@ -100,7 +104,16 @@ void tg_params_init(tg_params* p, int32_t vocab) {
   p->top_p = 1.0f;
 }
 
-tg_status tg_config_create(const tg_params* p, tg_config** out) {
+namespace {
+tg_status config_create(const tg_params* p, tg_config** out, tg_stream stream, bool with_plain);
+}
+
+tg_status tg_config_create(const tg_params* p, tg_config** out, tg_stream stream) {
+  return config_create(p, out, stream, true);
+}
+
+namespace {
+tg_status config_create(const tg_params* p, tg_config** out, tg_stream stream, bool with_plain) {
   if (!p || !out) return TG_ERR_INVALID_ARGUMENT;
   *out = nullptr;
   const int32_t V = p->vocab;
@@ -192,7 +205,8 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   size_t o_tick = o; o += cfg->max_batch;
   size_t o_status = o; o += 1;
   size_t o_slow = ((o * 4 + 15) / 16) * 16 / 4;
-  e = cudaMemcpy(cfg->dmem, host.data(), bytes, cudaMemcpyHostToDevice);
+  e = cudaMemcpyAsync(cfg->dmem, host.data(), bytes, cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) { cudaFree(cfg->dmem); delete cfg; return from_cuda(e); }
 
   int* d = static_cast<int*>(cfg->dmem);
@@ -240,6 +254,20 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
     if (e != cudaSuccess) st = from_cuda(e);
     else if (cfg->state_smem > optin || cfg->proc_smem > optin) st = TG_ERR_UNSUPPORTED;
   }
+  if (st == TG_OK && with_plain) {
+    tg_params q;
+    tg_params_init(&q, V);
+    q.mode = p->mode;
+    q.top_k = p->top_k;
+    q.top_p = p->top_p;
+    q.max_batch = p->max_batch;
+    st = config_create(&q, &cfg->plain, stream, false);
+    if (st == TG_OK) {
+      // its launches report in this config's status word and slow-row count
+      cfg->plain->dev.status = cfg->dev.status;
+      cfg->plain->dev.slow_rows = cfg->dev.slow_rows;
+    }
+  }
   if (st != TG_OK) {
     cudaFree(cfg->dmem);
     delete cfg;
@@ -248,14 +276,27 @@ tg_status tg_config_create(const tg_params* p, tg_config** out) {
   *out = cfg;
   return TG_OK;
 }
+}  // namespace
 
 tg_status tg_config_destroy(tg_config* cfg) {
   if (!cfg) return TG_ERR_INVALID_ARGUMENT;
   cudaError_t e = cudaDeviceSynchronize();
   cudaError_t e2 = cudaFree(cfg->dmem);
+  if (cfg->plain) {
+    const tg_status s2 = tg_config_destroy(cfg->plain);
+    if (e2 == cudaSuccess && s2 != TG_OK) e2 = cudaErrorUnknown;
+  }
   delete cfg;
   return from_cuda(e != cudaSuccess ? e : e2);
 }
+
+tg_status tg_config_view(const tg_config* cfg, void* out, size_t size) {
+  if (!cfg || !out || size != sizeof(tg::DevCfg)) return TG_ERR_INVALID_ARGUMENT;
+  std::memcpy(out, &cfg->dev, sizeof(tg::DevCfg));
+  return TG_OK;
+}
+
+const tg_config* tg_config_selection(const tg_config* cfg) { return cfg ? cfg->plain : nullptr; }
 
 namespace {
 tg_status select_impl(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
@@ -479,6 +520,11 @@ tg_status tg_query_status(const tg_config* cfg, uint32_t* flags, uint64_t* slow_
   if (flags) *flags = f;
   if (slow_rows) *slow_rows = s;
   return TG_OK;
+}
+
+tg_status tg_status_word(const tg_config* cfg, uint32_t* flags) {
+  if (!flags) return TG_ERR_INVALID_ARGUMENT;
+  return tg_query_status(cfg, flags, nullptr);
 }
 
 tg_status tg_clear_status(const tg_config* cfg) {

@@ -36,7 +36,8 @@ TG_MAX_STATE_COLS = 4096
 EXPORTS = ("tg_params_init", "tg_config_create", "tg_config_destroy", "tg_select", "tg_select_logprobs", "tg_verify",
            "tg_process", "tg_query_status", "tg_clear_status", "tg_next_num_candidates",
            "tg_status_string", "tg_verify_noalloc", "tg_beam_step", "tg_beam_keep",
-           "tg_verify_history", "tg_select_state", "tg_process_state", "tg_set_wait_limit")
+           "tg_verify_history", "tg_select_state", "tg_process_state", "tg_set_wait_limit", "tg_status_word",
+           "tg_config_view", "tg_config_selection")
 TG_NOALLOC_MAX_BATCH = 1024
 
 
@@ -99,7 +100,9 @@ def load_library(path: str | None = None):
     lib = ctypes.CDLL(path)
     lib.tg_params_init.argtypes = [POINTER(tg_params), c_int32]
     lib.tg_params_init.restype = None
-    lib.tg_config_create.argtypes = [POINTER(tg_params), POINTER(c_void_p)]
+    lib.tg_config_create.argtypes = [POINTER(tg_params), POINTER(c_void_p), c_void_p]
+    lib.tg_status_word.argtypes = [c_void_p, POINTER(c_uint32)]
+    lib.tg_status_word.restype = c_int
     lib.tg_config_destroy.argtypes = [c_void_p]
     lib.tg_select.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p]
@@ -215,11 +218,13 @@ def make_params(vocab: int, logits_dtype="f32", mode="greedy", repetition_penalt
 class Config:
     """Owns a tg_config* (tg_config_create / tg_config_destroy)."""
 
-    def __init__(self, **params):
+    def __init__(self, stream=None, **params):
         lib = load_library()
         p, keep = make_params(**params)
         h = c_void_p()
-        _check("tg_config_create", lib.tg_config_create(ctypes.byref(p), ctypes.byref(h)))
+        # the uploads go on `stream` (a torch stream), or on the default stream
+        st = c_void_p(stream.cuda_stream) if stream is not None else None
+        _check("tg_config_create", lib.tg_config_create(ctypes.byref(p), ctypes.byref(h), st))
         self.handle = h
         self.params = dict(params)
         del keep
@@ -473,6 +478,13 @@ def tg_query_status(cfg: Config):
     f, s = c_uint32(), c_uint64()
     _check("tg_query_status", load_library().tg_query_status(cfg.handle, ctypes.byref(f), ctypes.byref(s)))
     return int(f.value), int(s.value)
+
+
+def tg_status_word(cfg: Config) -> int:
+    """The sticky status bits (synchronous)."""
+    f = c_uint32()
+    _check("tg_status_word", load_library().tg_status_word(cfg.handle, ctypes.byref(f)))
+    return int(f.value)
 
 
 def tg_clear_status(cfg: Config):

@@ -16,7 +16,9 @@ What it computes, step by step, in the order the pages give:
 * Same page, section "Processors": a processor is a per-row state made on the
   host before each step plus a function of the row's scores and that state;
   the task's come at the end of the list.  Here the functions are "bias"
-  (s + v) and "set" (v) over a sparse state of (id, value) entries.
+  (s + v) and "set" (v) over a sparse state of (id, value) entries, or one
+  function given by the caller (``Params.custom``: the row's scores and its
+  dense state row in, new scores out; f32, never below the filter value).
 * Same page, section "Lengths": a row's length L counts the prompt and the new
   tokens; max_length = prompt + max_new_tokens; the rules for
   no_repeat_ngram_size, min_length, min_new_tokens, forced_bos, forced_eos and
@@ -102,6 +104,9 @@ class Params:
     # the task's processors: (kind, size) pairs, kind "bias" (s + v) or "set" (v); each owns
     # `size` columns of the per-row state (ids, values) passed next to the logits
     processors: Sequence[tuple] = ()
+    # or one task processor given as a function (scores [V] f32, state row) -> new scores [V];
+    # the state passed next to the logits is then a dense [B, S] array
+    custom: object = None
 
 
 @dataclass
@@ -312,6 +317,8 @@ def process_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, state=None):
     # the task's processors, at the end of the list
     if p.processors:
         apply_processors(s, state, p, info)
+    if p.custom is not None:
+        s = _clamp(np.asarray(p.custom(s.copy(), state), dtype=np.float32))
     return s, banned, info
 
 
@@ -442,7 +449,11 @@ def select_row(x: np.ndarray, h: Sequence[int], P: int, p: Params, u: float, sta
 
 
 def _row_state(proc_state, r):
-    return None if proc_state is None else (proc_state[0][r], proc_state[1][r])
+    if proc_state is None:
+        return None
+    if isinstance(proc_state, np.ndarray):   # a dense state (Params.custom)
+        return proc_state[r]
+    return (proc_state[0][r], proc_state[1][r])
 
 
 def select(logits, hist_ids, hist_offsets, prompt_lens, p: Params, uniforms=None,

@@ -87,7 +87,7 @@ def test_config_create_rejects_bad_params_on_host(lib):
     for kw in bad:
         p, keep = tg.make_params(**kw)
         h = ctypes.c_void_p()
-        st = lib.tg_config_create(ctypes.byref(p), ctypes.byref(h))
+        st = lib.tg_config_create(ctypes.byref(p), ctypes.byref(h), None)
         want = tg.TG_ERR_UNSUPPORTED if kw.get("vocab", 0) > tg.TG_MAX_VOCAB else tg.TG_ERR_INVALID_ARGUMENT
         assert st == want, kw
 
@@ -143,7 +143,7 @@ def test_config_create_rejects_bad_processors_on_host(lib):
     for kw in bad:
         p, keep = tg.make_params(vocab=10, **kw)
         h = ctypes.c_void_p()
-        assert lib.tg_config_create(ctypes.byref(p), ctypes.byref(h)) == tg.TG_ERR_INVALID_ARGUMENT, kw
+        assert lib.tg_config_create(ctypes.byref(p), ctypes.byref(h), None) == tg.TG_ERR_INVALID_ARGUMENT, kw
 
 
 def test_state_entry_points_reject_null_arguments(lib):
@@ -179,3 +179,11 @@ def test_status_flags_agree_across_header_binding_and_kernels():
     assert raised == set(declared.values())
     for name, value in declared.items():
         assert getattr(T, "TG_FLAG_" + name) == value
+
+
+def test_task_processor_header_compiles(tmp_path):
+    # include/tg_custom.cuh instantiated with a functor, as a caller would build it
+    from tests import custom_build
+    out = os.path.join(str(tmp_path), "task_processor.o")
+    r = subprocess.run(custom_build.nvcc_cmd(out, shared=False), capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -129,6 +129,7 @@ def test_out_of_range_history_ids_flagged():
         w.hist_ids[::3] = np.where(np.arange(w.hist_ids[::3].size) % 2, -5, 500)
     gpu, cfg, _ = compare_select(w)
     flags, _ = tg.tg_query_status(cfg)
+    assert tg.tg_status_word(cfg) == flags
     assert flags & tg.TG_FLAG_HISTORY_ID_OUT_OF_RANGE
 
 

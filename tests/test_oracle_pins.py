@@ -890,3 +890,52 @@ def test_log_softmax_at_closed_forms():
     assert abs(O.log_softmax_at(s, 0) - math.log(0.25)) < 1e-7
     # every token at the filter value: uniform over V
     assert abs(O.log_softmax_at(np.full(5, F, np.float32), 3) + math.log(5.0)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# A task processor given as a function (Params.custom) of the row's scores and
+# its dense state row, at the same place in the list as the sparse kinds
+# --------------------------------------------------------------------------
+def test_custom_processor_identity_changes_nothing():
+    rng = np.random.default_rng(71)
+    B, V = 6, 300
+    logits = rng.normal(0, 2, (B, V)).astype(np.float32)
+    lens = rng.integers(1, 20, B)
+    ids = rng.integers(0, V, int(lens.sum())).astype(np.int32)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    plen = np.maximum(1, lens // 2).astype(np.int32)
+    u = rng.random(B).astype(np.float32)
+    kw = dict(vocab=V, mode="sample", repetition_penalty=1.3, top_p=0.8)
+    a = O.select(logits, ids, off, plen, P(**kw), u)[0]
+    b = O.select(logits, ids, off, plen, P(**kw, custom=lambda s, row: s), u,
+                 proc_state=np.zeros((B, 4), np.float32))[0]
+    assert np.array_equal(a, b)
+
+
+def test_custom_dense_bias_equals_the_sparse_bias_kind():
+    # the same bias written both ways: a function adding row[i] to every token,
+    # and the "bias" kind listing every token with that value
+    rng = np.random.default_rng(72)
+    V = 40
+    x = rng.normal(0, 2, V).astype(np.float32)
+    h = [3, 3, 8, 11]
+    bias = rng.normal(0, 1, V).astype(np.float32)
+    kw = dict(vocab=V, repetition_penalty=1.2, suppress_tokens=[5], eos_token_ids=[2], min_length=10)
+    s1, _, _ = O.process_row(x, h, 2, P(**kw, custom=lambda s, row: s + row), bias)
+    s2, _, _ = O.process_row(x, h, 2, P(**kw, processors=(("bias", V),)),
+                             (np.arange(V, dtype=np.int32), bias))
+    assert np.array_equal(s1, s2)
+
+
+def test_custom_processor_runs_after_suppress_and_before_temperature():
+    V = 8
+    x = np.zeros(V, np.float32)
+    # it brings a suppressed token back (it runs after suppress_tokens) ...
+    keep7 = lambda s, row: np.where(np.arange(V) == 7, np.float32(row[0]), s)
+    s, banned = O.processed_scores(x, [1], 1, P(vocab=V, suppress_tokens=[7], custom=keep7),
+                                   np.array([1.5], np.float32))
+    assert s[7] == np.float32(1.5) and banned[7]
+    # ... and the temperature divides what it gives
+    s, _ = O.processed_scores(x, [1], 1, P(vocab=V, mode="sample", temperature=0.5, custom=keep7),
+                              np.array([3.0], np.float32))
+    assert s[7] == 6.0 and s[0] == 0.0
