@@ -32,6 +32,15 @@
  *  scores  device f32 [B, V] scratch.
  * Errors: TG_ERR_INVALID_ARGUMENT for a bad argument or a config with the
  * sparse processor kinds (those run in tg_select_state), TG_ERR_CUDA.
+ *
+ * tg_verify_custom<Proc>(...) is assisted-generation verify (Assisted
+ * Generation, steps 3-5) with the task processor at every one of the K+1
+ * positions of each row: position j of row b is target row b (K+1) + j, with
+ * state row b (K+1) + j (state: device f32 [B (K+1), S], or NULL with S = 0);
+ * as in tg_verify, the history processors do not run per position.  Its
+ * scores (then the temperature) go to `scores` (device f32 [B (K+1), V]) and
+ * tg_verify selects from them with tg_config_selection(cfg).  Arguments as
+ * tg_verify otherwise.
  */
 #pragma once
 
@@ -44,7 +53,9 @@ namespace tg_custom {
 
 constexpr int kThreads = tg::kThreads;
 
-template <int DT, class Proc>
+// HIST: the rows have histories and the built-in processors run (select);
+// otherwise every row is a verify position and only the task's function runs.
+template <int DT, class Proc, bool HIST>
 __global__ void __launch_bounds__(kThreads) task_scores_kernel(const tg::DevCfg c, const void* logits, int B, int V,
                                                                const int32_t* hist, const int64_t* off,
                                                                const int32_t* plen, const float* state, int S,
@@ -54,25 +65,29 @@ __global__ void __launch_bounds__(kThreads) task_scores_kernel(const tg::DevCfg 
   unsigned* H = reinterpret_cast<unsigned*>(smem_raw);
   unsigned* N = H + (nwords * 4 + 127) / 128 * 32;
   const int row = static_cast<int>(blockIdx.x);
-  const tg::RowMeta rm = tg::row_meta(c, hist, off, plen, row, B);
-  if (rm.bad || rm.L == 0) return;   // the selection gives these rows -1
-  tg::build_row_bitmaps(c, hist, rm, H, N, nwords);
+  tg::RowMeta rm{};
   int zs[8];
-  const int nz = rm.forced ? tg::forced_zeros(c, rm, zs) : 0;
+  int nz = 0;
+  if (HIST) {
+    rm = tg::row_meta(c, hist, off, plen, row, B);
+    if (rm.bad || rm.L == 0) return;   // the selection gives these rows -1
+    tg::build_row_bitmaps(c, hist, rm, H, N, nwords);
+    nz = rm.forced ? tg::forced_zeros(c, rm, zs) : 0;
+  }
   const float* st = state ? state + static_cast<size_t>(row) * S : nullptr;
   const bool tempered = c.mode == tg::kSample && c.temp != 1.0f;
   const unsigned char* rowp = static_cast<const unsigned char*>(logits) + static_cast<size_t>(row) * V * (DT == tg::kF32 ? 4 : 2);
   float* out = scores + static_cast<size_t>(row) * V;
   for (int i = threadIdx.x; i < V; i += kThreads) {
     float s;
-    if (rm.forced) {
+    if (HIST && rm.forced) {
       s = tg::kFilter;
       for (int q = 0; q < nz; ++q) s = zs[q] == i ? 0.0f : s;
     } else {
       const float x = DT == tg::kF32
                           ? __ldg(reinterpret_cast<const float*>(rowp) + i)
                           : __uint_as_float(static_cast<unsigned>(__ldg(reinterpret_cast<const unsigned short*>(rowp) + i)) << 16);
-      s = tg::process_elem(c, H, N, x, i, false);
+      s = HIST ? tg::process_elem(c, H, N, x, i, false) : x;
     }
     s = tg::clampf(proc(s, i, st, S));
     if (tempered) s = tg::clampf(__fdiv_rn(s, c.temp));
@@ -93,21 +108,35 @@ inline tg_status tg_select_custom(const void* logits, int32_t B, int32_t V, cons
   const int nwords = (V + 31) / 32;
   const int smem = 2 * ((nwords * 4 + 127) / 128 * 128);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (c.dtype == tg::kF32) {
-    auto k = task_scores_kernel<tg::kF32, Proc>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return TG_ERR_CUDA;
-    k<<<B, kThreads, smem, s>>>(c, logits, B, V, hist_ids, hist_offsets, prompt_lens, state, S, scores, proc);
-  } else {
-    auto k = task_scores_kernel<tg::kBF16, Proc>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return TG_ERR_CUDA;
-    k<<<B, kThreads, smem, s>>>(c, logits, B, V, hist_ids, hist_offsets, prompt_lens, state, S, scores, proc);
-  }
+  auto k = c.dtype == tg::kF32 ? task_scores_kernel<tg::kF32, Proc, true> : task_scores_kernel<tg::kBF16, Proc, true>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return TG_ERR_CUDA;
+  k<<<B, kThreads, smem, s>>>(c, logits, B, V, hist_ids, hist_offsets, prompt_lens, state, S, scores, proc);
   if (cudaGetLastError() != cudaSuccess) return TG_ERR_CUDA;
   const tg_config* sel = tg_config_selection(cfg);
   if (out_logprobs)
     return tg_select_logprobs(scores, B, V, hist_ids, hist_offsets, prompt_lens, sel, uniforms, out_ids, out_logprobs,
                               stream);
   return tg_select(scores, B, V, hist_ids, hist_offsets, prompt_lens, sel, uniforms, out_ids, stream);
+}
+
+template <class Proc>
+inline tg_status tg_verify_custom(const void* target_logits, int32_t B, int32_t V, const int32_t* cand_ids, int32_t K,
+                                  const tg_config* cfg, const float* state, int32_t S, const float* uniforms,
+                                  float* scores, int32_t* out_match, int32_t* out_next, tg_stream stream,
+                                  Proc proc = Proc()) {
+  tg::DevCfg c;
+  if (!cfg || tg_config_view(cfg, &c, sizeof(c)) != TG_OK) return TG_ERR_INVALID_ARGUMENT;
+  if (c.nproc > 0 || B < 0 || K < 1 || V != c.V || S < 0 || (S > 0) != (state != nullptr))
+    return TG_ERR_INVALID_ARGUMENT;
+  if (B == 0) return TG_OK;
+  if (!target_logits || !cand_ids || !scores || !out_match || !out_next) return TG_ERR_INVALID_ARGUMENT;
+  if (static_cast<long long>(B) * (K + 1) > 0x7fffffffLL) return TG_ERR_INVALID_ARGUMENT;
+  const int rows = B * (K + 1);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto k = c.dtype == tg::kF32 ? task_scores_kernel<tg::kF32, Proc, false> : task_scores_kernel<tg::kBF16, Proc, false>;
+  k<<<rows, kThreads, 0, s>>>(c, target_logits, rows, V, nullptr, nullptr, nullptr, state, S, scores, proc);
+  if (cudaGetLastError() != cudaSuccess) return TG_ERR_CUDA;
+  return tg_verify(scores, B, V, cand_ids, K, tg_config_selection(cfg), uniforms, out_match, out_next, stream);
 }
 
 }  // namespace tg_custom

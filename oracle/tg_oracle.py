@@ -562,12 +562,13 @@ def beam_candidates(logits, beam_scores, hist_ids, hist_offsets, prompt_lens, nu
 # ---------------------------------------------------------------------------
 # Assisted generation verify (steps 2-5) and the candidate heuristic (step 6)
 # ---------------------------------------------------------------------------
-def verify(target_logits, cand_ids, K: int, p: Params, uniforms=None):
+def verify(target_logits, cand_ids, K: int, p: Params, uniforms=None, proc_state=None):
     """tg_verify: select at each of the K+1 positions, count left-to-right
     matches, keep the matches plus the first divergent token.
 
     Position j selects from target_logits[b, j] with the warpers only (no
-    history processors run per position).
+    history processors run per position); with Params.custom, the task's
+    function first, with state row b (K+1) + j of proc_state.
     """
     B = target_logits.shape[0]
     out_match = np.zeros(B, dtype=np.int32)
@@ -578,6 +579,8 @@ def verify(target_logits, cand_ids, K: int, p: Params, uniforms=None):
         row_infos = []
         for j in range(K + 1):
             x = upcast_row(target_logits[b, j], p.logits_dtype)
+            if p.custom is not None:
+                x = _clamp(np.asarray(p.custom(x.copy(), proc_state[b * (K + 1) + j]), dtype=np.float32))
             if p.mode == "greedy":
                 nxt.append(int(np.argmax(x)))
                 row_infos.append(RowInfo())

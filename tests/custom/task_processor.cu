@@ -16,3 +16,10 @@ extern "C" int task_select(const void* logits, int B, int V, const int32_t* hist
                                      static_cast<const tg_config*>(cfg), state, S, uniforms, scores, out_ids,
                                      out_logprobs, static_cast<tg_stream>(stream), BucketBias());
 }
+
+extern "C" int task_verify(const void* target, int B, int V, const int32_t* cand, int K, const void* cfg,
+                           const float* state, int S, const float* uniforms, float* scores, int32_t* out_match,
+                           int32_t* out_next, void* stream) {
+  return tg_custom::tg_verify_custom(target, B, V, cand, K, static_cast<const tg_config*>(cfg), state, S, uniforms,
+                                     scores, out_match, out_next, static_cast<tg_stream>(stream), BucketBias());
+}

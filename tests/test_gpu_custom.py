@@ -87,3 +87,40 @@ def test_task_processor_zero_state_is_plain_select(task_lib):
     ids, _, _ = run(task_lib, w, np.zeros((w.B, 16), np.float32), logprobs=False)
     plain, _ = gpu_select(w)
     assert np.array_equal(ids, plain)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_task_processor_in_verify(task_lib, mode):
+    import torch
+    import logits_processing_token_gb300 as tg
+    B, K, S = 8, 5, 32
+    w = W.config4(B=B, K=K, mode=mode)
+    if mode == "sample":
+        w.params.update(temperature=0.8, top_p=0.9)
+    tgt = np.ascontiguousarray(w.extra["target"])
+    greedy = tgt.argmax(axis=-1)[:, :K]
+    cand = W.make_candidates(greedy, w.extra["agree"], w.extra["offsets"], w.V)
+    state = np.random.default_rng(98).normal(0.0, 1.0, (B * (K + 1), S)).astype(np.float32)
+    cfg = tg.Config(**w.params)
+    t = torch.from_numpy(tgt).cuda()
+    c = torch.from_numpy(cand).cuda()
+    u = torch.from_numpy(np.ascontiguousarray(w.uniforms)).cuda()
+    st = torch.from_numpy(state).cuda()
+    scores = torch.empty((B * (K + 1), w.V), dtype=torch.float32, device="cuda")
+    om = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    on = torch.full((B, K + 1), -9, dtype=torch.int32, device="cuda")
+    p = ctypes.c_void_p
+    rc = task_lib.task_verify(p(t.data_ptr()), B, w.V, p(c.data_ptr()), K, cfg.handle, p(st.data_ptr()), S,
+                              p(u.data_ptr()), p(scores.data_ptr()), p(om.data_ptr()), p(on.data_ptr()),
+                              p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    om, on = om.cpu().numpy(), on.cpu().numpy()
+    po = O.Params(**w.params, custom=bucket_bias(S, w.V))
+    m_ref, n_ref, infos = O.verify(tgt, cand, K, po, w.uniforms, proc_state=state)
+    for b in range(B):
+        upto = int(m_ref[b])
+        if any(ri.u_boundary or ri.topp_boundary for ri in infos[b][1][:upto + 1]):
+            continue
+        assert om[b] == m_ref[b], (b, om[b], m_ref[b])
+        assert list(on[b]) == list(n_ref[b])
