@@ -80,3 +80,23 @@ def test_select_after_timeout():
     assert tg.tg_query_status(cfg)[0] & tg.TG_FLAG_TIMEOUT
     assert (o == -1).any() and not (o == -9).any()
     compare_select(w)
+
+
+def test_verify_history_after_timeout():
+    import logits_processing_token_gb300 as tg
+    from tests.test_gpu_verify import run_gpu_history
+    B, K = 6, 4
+    w, tgt, cand, p = make_case(B, K, "greedy", repetition_penalty=1.5, no_repeat_ngram_size=3)
+    rng = np.random.default_rng(5)
+    hists = [list(rng.integers(0, 50, int(rng.integers(2, 30)))) for _ in range(B)]
+    plens = [1] * B
+    tg.tg_set_wait_limit(1)
+    try:
+        om, _, _, _ = run_gpu_history(w, tgt, cand, K, hists, plens)
+    finally:
+        tg.tg_set_wait_limit(0)
+    assert (om == -1).any() and not (om == -9).any()
+    om2, on2, ids, off = run_gpu_history(w, tgt, cand, K, hists, plens)
+    m_ref, n_ref, infos = O.verify_history(tgt, cand, K, ids, off, np.asarray(plens, np.int32), O.Params(**w.params),
+                                           w.uniforms)
+    assert np.array_equal(om2, m_ref) and np.array_equal(on2, n_ref)

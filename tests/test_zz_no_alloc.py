@@ -75,3 +75,42 @@ def test_noalloc_rejects_batch_above_maximum(lib):
                                ctypes.byref(params), None, ctypes.c_void_p(om.data_ptr()),
                                ctypes.c_void_p(on.data_ptr()), None)
     assert st == tg.TG_ERR_UNSUPPORTED
+
+
+def test_noalloc_after_timeout(lib):
+    # a launch whose bounded wait ran out writes -1 to the batch rows it did not
+    # finish (no status word is reported here); the next call is exact again
+    import torch
+    import logits_processing_token_gb300 as tg
+    B, K, V = 8, 5, 50_272
+    settings = dict(vocab=V, mode="greedy")
+    cfg = tg.Config(**settings, max_batch=64)
+    params, keep = tg.make_params(**settings)
+    tgt, cand, u = _case(B, K, V, "greedy", 7)
+    t = torch.from_numpy(tgt).cuda()
+    c = torch.from_numpy(cand).cuda()
+    uu = torch.from_numpy(u).cuda()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call():
+        om = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+        on = torch.full((B, K + 1), -9, dtype=torch.int32, device="cuda")
+        st = lib.tg_verify_noalloc(ctypes.c_void_p(t.data_ptr()), B, V, ctypes.c_void_p(c.data_ptr()), K,
+                                   ctypes.byref(params), ctypes.c_void_p(uu.data_ptr()),
+                                   ctypes.c_void_p(om.data_ptr()), ctypes.c_void_p(on.data_ptr()), stream)
+        assert st == tg.TG_OK
+        torch.cuda.synchronize()
+        return om.cpu().numpy(), on.cpu().numpy()
+
+    tg.tg_set_wait_limit(1)
+    try:
+        om, _ = call()
+    finally:
+        tg.tg_set_wait_limit(0)
+    assert (om == -1).any() and not (om == -9).any()
+    om2, on2 = call()
+    ref_m = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    ref_n = torch.full((B, K + 1), -9, dtype=torch.int32, device="cuda")
+    tg.tg_verify(t, c, K, cfg, uu, ref_m, ref_n)
+    torch.cuda.synchronize()
+    assert np.array_equal(om2, ref_m.cpu().numpy()) and np.array_equal(on2, ref_n.cpu().numpy())
