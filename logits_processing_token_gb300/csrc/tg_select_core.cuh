@@ -281,6 +281,44 @@ struct RowGlobalSource {
     }
     for (int i = done + static_cast<int>(threadIdx.x); i < V; i += kThreads) f(score(load_logit<DT>(row, i), i), static_cast<unsigned>(i));
   }
+  // pass() with eight vectors in flight per thread and the per-vector work
+  // unrolled, for a row read again at the end of its finish (from L2 or
+  // HBM, latency-bound at four vectors).  A small f only: it is inlined
+  // eight times.
+  template <class Fn>
+  __device__ __forceinline__ void pass_deep(Fn f) const {
+    constexpr int PER = DT == kF32 ? 4 : 8;
+    constexpr int NV = 8;
+    if (sparse || (reinterpret_cast<uintptr_t>(row) & 15u) != 0u) {
+      pass(f);
+      return;
+    }
+    const int nvec = V / PER;
+    const uint4* rv = static_cast<const uint4*>(row);
+    for (int v0 = 0; v0 < nvec; v0 += NV * kThreads) {
+      uint4 q[NV];
+#pragma unroll
+      for (int h = 0; h < NV; ++h) {
+        const int vi = v0 + h * kThreads + static_cast<int>(threadIdx.x);
+        q[h] = vi < nvec ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int h = 0; h < NV; ++h) {
+        const int vi = v0 + h * kThreads + static_cast<int>(threadIdx.x);
+        if (vi < nvec) {
+          const unsigned ps[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+#pragma unroll
+          for (int e = 0; e < PER; ++e) {
+            const float x = DT == kF32 ? __uint_as_float(ps[e]) : ((e & 1) ? bf16hi(ps[e >> 1]) : bf16lo(ps[e >> 1]));
+            const int i = vi * PER + e;
+            f(score(x, i), static_cast<unsigned>(i));
+          }
+        }
+      }
+    }
+    for (int i = nvec * PER + static_cast<int>(threadIdx.x); i < V; i += kThreads)
+      f(score(load_logit<DT>(row, i), i), static_cast<unsigned>(i));
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -1502,24 +1540,37 @@ __device__ __noinline__ FinResult tail_pick(const DevCfg& c, const SelArgs& a, S
   if (Td < Zc) { res.reason = 41; return res; }
   const unsigned long long R = Td - Zc;   // the draw's target within the tail
   TG_TF(19);
-  static_assert(kEvCap * 4 >= kLevels * 8, "tail histogram");
-  unsigned long long* hm = reinterpret_cast<unsigned long long*>(sm.ev);
-  for (int l = tid; l < kLevels; l += kThreads) hm[l] = 0ull;
+  // each bin's mass in two 32-bit words: the low words of the weights, and
+  // their high words plus one for every add that carried out of the low word
+  // (the thread whose add wrapped sees it in the value the atomic returns).
+  // A tail weight is below 2^44 and V <= 2^18, so the high word stays below 2^32.
+  static_assert(kEvCap >= 2 * kLevels, "tail histogram");
+  unsigned* hlo = sm.ev;
+  unsigned* hhi = sm.ev + kLevels;
+  for (int l = tid; l < kLevels; l += kThreads) { hlo[l] = 0u; hhi[l] = 0u; }
   if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, reinterpret_cast<int*>(sm.cand_s), 2 * kCandCap);
   else csync();
   const float hi = theta_f, lo = m - 32.0f;
   const float scale = hi > lo ? static_cast<float>(kLevels) / (hi - lo) : 0.0f;
   auto bin = [&](float s) { return min(max(static_cast<int>((hi - s) * scale), 0), kLevels - 1); };
   RowGlobalSource<DT> src{rowp, a.V, &c, M, N, bitmaps, true};
-  src.pass([&](float s, unsigned) {
-    if (s < hi) atomicAdd(&hm[bin(s)], wfix_fast(s, cc));
+  src.pass_deep([&](float s, unsigned) {
+    if (s < hi) {
+      const unsigned long long w = wfix_fast(s, cc);
+      const int b = bin(s);
+      const unsigned wl = static_cast<unsigned>(w);
+      const unsigned old = atomicAdd(&hlo[b], wl);
+      const unsigned wh = static_cast<unsigned>(w >> 32) + (old + wl < old ? 1u : 0u);
+      if (wh) atomicAdd(&hhi[b], wh);
+    }
   });
   csync();
   TG_TF(20);
   // bins 2t and 2t+1 per thread: the tail's mass before them, then the bin
   // whose running mass first passes R
   const int l0 = 2 * tid, l1 = l0 + 1;
-  const unsigned long long m0 = hm[l0], m1 = hm[l1];
+  const unsigned long long m0 = (static_cast<unsigned long long>(hhi[l0]) << 32) + hlo[l0];
+  const unsigned long long m1 = (static_cast<unsigned long long>(hhi[l1]) << 32) + hlo[l1];
   unsigned long long im = m0 + m1;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1543,7 +1594,7 @@ __device__ __noinline__ FinResult tail_pick(const DevCfg& c, const SelArgs& a, S
   if (tid == 0) sm.misc.ncand = 0;
   csync();
   float smax = -INFINITY, smin = INFINITY;
-  src.pass([&](float s, unsigned t) {
+  src.pass_deep([&](float s, unsigned t) {
     if (s < hi && bin(s) == bs) {
       const int pos = atomicAdd(&sm.misc.ncand, 1);
       if (pos < kCandCap) { sm.cand_s[pos] = s; sm.cand_i[pos] = t; }
