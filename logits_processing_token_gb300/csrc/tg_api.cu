@@ -24,6 +24,10 @@ struct tg_config {
   int dtype = 0;
   int mode = 0;
   int max_batch = 0;
+  // greedy ids of a small batch over several CTAs per row: one key and one
+  // count per row (tg::launch_split_greedy), in dmem, zero between calls
+  unsigned long long* split_best = nullptr;
+  unsigned* split_tick = nullptr;
   int nwords = 0;
   LaunchPlan sel, ver;
   int proc_smem = 0;
@@ -58,6 +62,10 @@ std::vector<int> sorted_unique(std::initializer_list<std::pair<const int32_t*, i
   v.erase(std::unique(v.begin(), v.end()), v.end());
   return v;
 }
+
+// The split greedy path: bytes of logits per CTA, and at most this many CTAs per row.
+constexpr long long kSplitSliceBytes = 16 * 1024;
+constexpr long long kSplitMaxSlices = 32;
 
 // Pick the TMA ring depth.  One CTA per SM (512 threads at 128 registers
 // fill the register file); three stages of 32 KB keep a row's stream fed, and
@@ -193,9 +201,10 @@ tg_status config_create(const tg_params* p, tg_config** out, tg_stream stream, b
   std::vector<int> feos = sorted_unique({{p->forced_eos_token_ids, p->n_forced_eos_token_ids}});
 
   // one allocation: [ban][sup][bsup][seq ids][seq offsets][tickets][status u32][pad][slow_rows u64]
+  // [split keys u64 x max_batch][split counts u32 x max_batch]
   const size_t n_int = ban.size() + sup.size() + bsup.size() + seq_ids.size() + seq_off.size() +
                        static_cast<size_t>(cfg->max_batch) + 2;
-  const size_t bytes = ((n_int * 4 + 15) / 16) * 16 + 16;
+  const size_t bytes = ((n_int * 4 + 15) / 16) * 16 + 16 + static_cast<size_t>(cfg->max_batch) * 12;
   e = cudaMalloc(&cfg->dmem, bytes);
   if (e != cudaSuccess) { delete cfg; return from_cuda(e); }
   std::vector<int> host(bytes / 4, 0);
@@ -205,6 +214,8 @@ tg_status config_create(const tg_params* p, tg_config** out, tg_stream stream, b
   size_t o_tick = o; o += cfg->max_batch;
   size_t o_status = o; o += 1;
   size_t o_slow = ((o * 4 + 15) / 16) * 16 / 4;
+  const size_t o_sbest = o_slow + 2;                                        // 8-byte aligned
+  const size_t o_stick = o_sbest + 2 * static_cast<size_t>(cfg->max_batch);
   e = cudaMemcpyAsync(cfg->dmem, host.data(), bytes, cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) { cudaFree(cfg->dmem); delete cfg; return from_cuda(e); }
@@ -242,6 +253,8 @@ tg_status config_create(const tg_params* p, tg_config** out, tg_stream stream, b
   c.tickets = reinterpret_cast<unsigned*>(d + o_tick);
   c.status = reinterpret_cast<unsigned*>(d + o_status);
   c.slow_rows = reinterpret_cast<unsigned long long*>(d + o_slow);
+  cfg->split_best = reinterpret_cast<unsigned long long*>(d + o_sbest);
+  cfg->split_tick = reinterpret_cast<unsigned*>(d + o_stick);
 
   st = plan_select(c.dtype, false, cfg->nwords, &cfg->sel);
   if (st == TG_OK) st = plan_select(c.dtype, true, 0, &cfg->ver);
@@ -331,6 +344,18 @@ tg_status select_impl(const void* logits, int32_t B, int32_t V, const int32_t* h
   a.out = out_ids;
   a.nstage = cfg->sel.nstage;
   a.nwords = cfg->nwords;
+  if (!out_logprobs && cfg->mode == TG_GREEDY && B <= cfg->max_batch) {
+    // Greedy ids of a batch too small to fill the GPU: each row over several
+    // CTAs of about kSplitSliceBytes, when every CTA fits in one wave
+    const long long rb = static_cast<long long>(V) * (cfg->dtype == TG_DTYPE_BF16 ? 2 : 4);
+    const long long ns = std::min<long long>(kSplitMaxSlices, (rb + kSplitSliceBytes - 1) / kSplitSliceBytes);
+    if (ns >= 2 && static_cast<long long>(B) * ns <= cfg->nsm) {
+      const int slice_tok = static_cast<int>((V + ns - 1) / ns + 7) / 8 * 8;
+      const int nslice = (V + slice_tok - 1) / slice_tok;
+      return from_cuda(tg::launch_split_greedy(dev, a, nslice, slice_tok, cfg->split_best, cfg->split_tick,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+    }
+  }
   int grid = std::min<long long>(B, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm);
   return from_cuda(tg::launch_select(dev, a, false, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -535,6 +560,7 @@ tg_status tg_clear_status(const tg_config* cfg) {
   if (e == cudaSuccess) e = cudaMemset(cfg->dev.slow_rows, 0, sizeof(unsigned long long));
   // tickets a launch left behind (one whose bounded wait ran out) start at zero again
   if (e == cudaSuccess) e = cudaMemset(cfg->dev.tickets, 0, static_cast<size_t>(cfg->max_batch) * sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(cfg->split_best, 0, static_cast<size_t>(cfg->max_batch) * 12);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return from_cuda(e);
 }

@@ -1076,6 +1076,160 @@ int state_smem_bytes(int nwords, int S) {
   return ring_offset(nwords) + bitmap_bytes(nwords) + state_stage_bytes(S) + sparse_list_bytes(S);
 }
 
+// ---------------------------------------------------------------------------
+// Greedy ids for a batch too small to fill the GPU: each row is split over
+// gridDim.x CTAs of slice_tok tokens (grid: slices x rows), so a few rows are
+// read by many SMs instead of one each.  Every CTA builds the row's bitmaps
+// (2 x V/8 bytes of shared memory), takes the best processed score of its
+// tokens with select_kernel's rules (the larger score, on a tie the smaller
+// id; a marked token competes with its processed score, an unmarked one with
+// its logit, and an unmarked -inf is never taken), and folds it into the
+// row's 64-bit key in global memory with atomicMax: order-preserving score
+// bits above the complemented id.  The last of the row's CTAs to count
+// itself in takes the key, leaves the key and the count at zero for the next
+// call, and writes the id.  No CTA waits for another.
+// ---------------------------------------------------------------------------
+constexpr int kSplitStage = 4096;   // history ids staged in shared memory (a longer history is read in place)
+struct SplitSmem {
+  float wf[kWarps];
+  unsigned wu[kWarps];
+};
+__host__ __device__ constexpr int split_stage_off() { return align_up(static_cast<int>(sizeof(SplitSmem)), 128); }
+__host__ __device__ constexpr int split_bits_off() { return align_up(split_stage_off() + kSplitStage * 4, 128); }
+__host__ __device__ constexpr int split_smem(int nwords) { return split_bits_off() + 2 * bitmap_bytes(nwords); }
+
+// Unsigned key in the order of the floats (no NaN reaches it).
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    split_greedy_kernel(const DevCfg c, const SelArgs a, int slice_tok, unsigned long long* best, unsigned* tick) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SplitSmem& ss = *reinterpret_cast<SplitSmem*>(smem_raw);
+  int* stage = reinterpret_cast<int*>(smem_raw + split_stage_off());
+  unsigned* M = reinterpret_cast<unsigned*>(smem_raw + split_bits_off());
+  unsigned* N = reinterpret_cast<unsigned*>(smem_raw + split_bits_off() + bitmap_bytes(a.nwords));
+  constexpr int esz = DT == kF32 ? 4 : 2;
+  constexpr int PER = 16 / esz;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int row = a.row_begin + static_cast<int>(blockIdx.y);
+  const int V = a.V;
+
+  // The logits and histories may come from the kernel before this one.
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
+  if (rm.bad || rm.L == 0 || rm.forced) {
+    // not read: the first slice writes the row's id
+    if (blockIdx.x == 0 && tid == 0) {
+      if (rm.bad || rm.L == 0) {
+        a.out[row] = -1;
+        if (rm.bad) atomicOr(c.status, kFlagBadRow);
+      } else {
+        unsigned long long kept = 1ull;
+        a.out[row] = forced_token(c, rm, V, 0.0f, false, &kept);
+      }
+    }
+    return;
+  }
+  const bool bitmaps = c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
+                       (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0));
+  if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, stage, kSplitStage);   // M = history | banned
+
+  const int t0 = static_cast<int>(blockIdx.x) * slice_tok;
+  const int t1 = min(V, t0 + slice_tok);
+  const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * esz;
+  float bv = -INFINITY;
+  unsigned bi = 0xffffffffu;
+  // a thread's tokens come in increasing id order
+  auto take = [&](float x, int i) {
+    if (bitmaps && get_bit(M, i)) {
+      const float s = process_elem(c, M, N, x, i, false);
+      if (s > bv || (s == bv && static_cast<unsigned>(i) < bi)) { bv = s; bi = static_cast<unsigned>(i); }
+    } else if (x > bv) {
+      bv = x;
+      bi = static_cast<unsigned>(i);
+    }
+  };
+  const bool vec = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0u) && ((static_cast<size_t>(V) * esz) % 16u == 0u);
+  if (vec) {
+    // whole 16-byte vectors (slice_tok is a multiple of 8 tokens), four in flight per thread
+    const uint4* rv = reinterpret_cast<const uint4*>(rowp);
+    const int v0 = t0 / PER, v1 = t1 / PER;
+    for (int vb = v0; vb < v1; vb += 4 * kThreads) {
+      uint4 q[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int vi = vb + h * kThreads + tid;
+        q[h] = vi < v1 ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int vi = vb + h * kThreads + tid;
+        if (vi < v1) {
+          const unsigned ps[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+#pragma unroll
+          for (int e = 0; e < PER; ++e)
+            take(DT == kF32 ? __uint_as_float(ps[e]) : ((e & 1) ? bf16hi(ps[e >> 1]) : bf16lo(ps[e >> 1])), vi * PER + e);
+        }
+      }
+    }
+  } else {
+    for (int i = t0 + tid; i < t1; i += kThreads) take(load_logit<DT>(rowp, i), i);
+  }
+  for (int o = 16; o; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+    const unsigned i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (v2 > bv || (v2 == bv && i2 < bi)) { bv = v2; bi = i2; }
+  }
+  if (lane == 0) { ss.wf[wid] = bv; ss.wu[wid] = bi; }
+  csync();
+  if (tid == 0) {
+    float v = ss.wf[0];
+    unsigned b = ss.wu[0];
+    for (int q = 1; q < kWarps; ++q) {
+      const float v2 = ss.wf[q];
+      const unsigned i2 = ss.wu[q];
+      if (v2 > v || (v2 == v && i2 < b)) { v = v2; b = i2; }
+    }
+    // no candidate: -inf over id 0xffffffff, below every real key, and the id -1 if no slice has one
+    atomicMax(best + row, (static_cast<unsigned long long>(order_key(v)) << 32) | static_cast<unsigned long long>(~b));
+    __threadfence();
+    const unsigned done = atomicAdd(tick + row, 1u);
+    if (done == gridDim.x - 1) {
+      __threadfence();
+      const unsigned long long k = atomicExch(best + row, 0ull);
+      tick[row] = 0u;
+      a.out[row] = static_cast<int>(~static_cast<unsigned>(k & 0xffffffffull));
+    }
+  }
+}
+
+template <int DT>
+static cudaError_t launch_split_t(const DevCfg& c, const SelArgs& a, int nslice, int slice_tok,
+                                  unsigned long long* best, unsigned* tick, cudaStream_t s) {
+  auto k = split_greedy_kernel<DT>;
+  const int smem = split_smem(a.nwords);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nslice), static_cast<unsigned>(a.nrows - a.row_begin));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, c, a, slice_tok, best, tick);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // One launch per kMaxRowsPerCta * grid rows; each is a programmatic dependent
 // of the kernel before it in the stream (its launch overlaps that kernel's
 // tail; it waits for it before touching global memory).
@@ -1114,6 +1268,16 @@ template <int DT>
 static cudaError_t launch_sel_v(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s) {
   if (!verify) return launch_sel_m<DT, 0>(c, a, grid, smem, s);
   return a.vhist ? launch_sel_m<DT, 2>(c, a, grid, smem, s) : launch_sel_m<DT, 1>(c, a, grid, smem, s);
+}
+
+int split_greedy_smem(int nwords) { return split_smem(nwords); }
+
+cudaError_t launch_split_greedy(const DevCfg& c, const SelArgs& a, int nslice, int slice_tok, unsigned long long* best,
+                                unsigned* tick, cudaStream_t s) {
+  if (nslice < 1 || slice_tok < 8 || slice_tok % 8 != 0 || a.nrows <= a.row_begin || a.nrows - a.row_begin > 65535)
+    return cudaErrorInvalidValue;
+  return c.dtype == kF32 ? launch_split_t<kF32>(c, a, nslice, slice_tok, best, tick, s)
+                         : launch_split_t<kBF16>(c, a, nslice, slice_tok, best, tick, s);
 }
 
 cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s) {

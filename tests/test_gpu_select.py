@@ -192,3 +192,73 @@ def test_multi_token_bad_words(mode):
         w.logits = w.logits.copy()
         w.logits[:, [5, 7, 11, 13, 17]] = 30.0
         compare_select(w, max_boundary_frac=0.34)
+
+
+# Greedy ids of a batch too small to fill the GPU run with each row split over
+# several CTAs (when batch x slices fits one wave of CTAs); the same rows in a
+# batch too large for that split run one row per CTA.  Both must give the
+# oracle's ids, and a second call on the same config the same ids again.
+SPLIT_CASES = [
+    # (V, dtype, B, overrides)
+    (50272, "f32", 1, dict(repetition_penalty=1.3, no_repeat_ngram_size=2)),
+    (50257, "bf16", 5, dict(repetition_penalty=1.2, no_repeat_ngram_size=3)),   # rows not on 16-byte boundaries
+    (151936, "bf16", 4, dict(suppress_tokens=list(range(0, 151936, 7)), repetition_penalty=0.9)),
+    (262144, "f32", 2, dict(repetition_penalty=0.7, eos_token_ids=[3], min_length=30)),
+    (20000, "f32", 7, {}),                                                        # no processors
+    (4104, "bf16", 9, dict(repetition_penalty=2.0)),                              # two slices of 2,056 tokens
+]
+
+
+def _replicated(w, B2):
+    hists = [np.asarray(w.history(b % w.B), np.int32) for b in range(B2)]
+    ids, off = W._pack(hists)
+    reps = (B2 + w.B - 1) // w.B
+    return W.Workload("replicated", dict(w.params), np.tile(w.logits, (reps, 1))[:B2], ids, off,
+                      np.tile(w.prompt_lens, reps)[:B2], np.tile(w.uniforms, reps)[:B2])
+
+
+@pytest.mark.parametrize("case", range(len(SPLIT_CASES)))
+def test_split_greedy_rows(case):
+    V, dtype, B, ov = SPLIT_CASES[case]
+    w = W.random_case(700 + case, B=B, V=V, dtype=dtype, mode="greedy", L_max=60, **ov)
+    gpu, cfg, _ = compare_select(w)
+    again, _ = gpu_select(w, cfg=cfg)
+    assert np.array_equal(again, gpu)
+    big, _ = gpu_select(_replicated(w, 160))
+    assert np.array_equal(big[:B], gpu)
+
+
+def test_split_greedy_forced_and_removed_rows():
+    # padding, forced bos, forced eos, begin-suppress and ordinary rows on a vocabulary that is split
+    V = 20000
+    rng = np.random.default_rng(14)
+    hists = [[], [11], [1, 2, 3, 4, 5], [9, 9, 9], [4, 5, 6, 7]]
+    plens = [0, 1, 2, 3, 1]
+    ids, off = W._pack([np.array(h, np.int32) for h in hists])
+    logits = rng.normal(0, 2, (len(hists), V)).astype(np.float32)
+    w = W.Workload("forced", _forced_params(V, mode="greedy"), logits, ids, off, np.array(plens, np.int32),
+                   rng.random(len(hists), dtype=np.float32))
+    gpu, _, _ = compare_select(w)
+    assert gpu[0] == -1
+    # every token suppressed: the filter value everywhere
+    w2 = W.random_case(15, B=4, V=10000, mode="greedy", suppress_tokens=list(range(10000)))
+    gpu2, _, _ = compare_select(w2)
+    assert all(g == 0 for g in gpu2 if g != -1)
+
+
+def test_split_greedy_unaligned_rows():
+    # logits that start 4 bytes past a 16-byte boundary: the split reads element by element
+    import torch
+    import logits_processing_token_gb300 as tg
+    w = W.random_case(16, B=3, V=50272, dtype="f32", mode="greedy", L_max=40, repetition_penalty=1.4)
+    dev = to_device(w)
+    buf = torch.empty(w.B * w.V + 1, dtype=torch.float32, device="cuda")
+    buf[1:].copy_(dev["logits"].reshape(-1))
+    shifted = buf[1:].view(w.B, w.V)
+    assert shifted.data_ptr() % 16 == 4
+    cfg = tg.Config(**w.params)
+    out = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    tg.tg_select(shifted, dev["hist_ids"], dev["hist_offsets"], dev["prompt_lens"], cfg, dev["uniforms"], out)
+    torch.cuda.synchronize()
+    ora, _ = oracle_select(w)
+    assert [int(x) for x in out.cpu().numpy()] == [int(x) for x in ora]
