@@ -312,6 +312,18 @@ tg_status tg_config_view(const tg_config* cfg, void* out, size_t size) {
 const tg_config* tg_config_selection(const tg_config* cfg) { return cfg ? cfg->plain : nullptr; }
 
 namespace {
+// Greedy ids of a batch too small to fill the GPU: each of the rows over
+// several CTAs of about kSplitSliceBytes, when every CTA fits in one wave.
+bool split_plan(const tg_config* cfg, long long rows, int* nslice, int* slice_tok) {
+  if (cfg->mode != TG_GREEDY || rows < 1 || rows > cfg->max_batch) return false;
+  const long long rb = static_cast<long long>(cfg->V) * (cfg->dtype == TG_DTYPE_BF16 ? 2 : 4);
+  const long long ns = std::min<long long>(kSplitMaxSlices, (rb + kSplitSliceBytes - 1) / kSplitSliceBytes);
+  if (ns < 2 || rows * ns > cfg->nsm) return false;
+  *slice_tok = static_cast<int>((cfg->V + ns - 1) / ns + 7) / 8 * 8;
+  *nslice = (cfg->V + *slice_tok - 1) / *slice_tok;
+  return true;
+}
+
 tg_status select_impl(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
                       const int64_t* hist_offsets, const int32_t* prompt_lens, const tg_config* cfg,
                       const float* uniforms, int32_t* out_ids, float* out_logprobs, tg_stream stream) {
@@ -344,18 +356,10 @@ tg_status select_impl(const void* logits, int32_t B, int32_t V, const int32_t* h
   a.out = out_ids;
   a.nstage = cfg->sel.nstage;
   a.nwords = cfg->nwords;
-  if (!out_logprobs && cfg->mode == TG_GREEDY && B <= cfg->max_batch) {
-    // Greedy ids of a batch too small to fill the GPU: each row over several
-    // CTAs of about kSplitSliceBytes, when every CTA fits in one wave
-    const long long rb = static_cast<long long>(V) * (cfg->dtype == TG_DTYPE_BF16 ? 2 : 4);
-    const long long ns = std::min<long long>(kSplitMaxSlices, (rb + kSplitSliceBytes - 1) / kSplitSliceBytes);
-    if (ns >= 2 && static_cast<long long>(B) * ns <= cfg->nsm) {
-      const int slice_tok = static_cast<int>((V + ns - 1) / ns + 7) / 8 * 8;
-      const int nslice = (V + slice_tok - 1) / slice_tok;
-      return from_cuda(tg::launch_split_greedy(dev, a, nslice, slice_tok, cfg->split_best, cfg->split_tick,
-                                               reinterpret_cast<cudaStream_t>(stream)));
-    }
-  }
+  int nslice = 0, slice_tok = 0;
+  if (!out_logprobs && split_plan(cfg, B, &nslice, &slice_tok))
+    return from_cuda(tg::launch_split_greedy(dev, a, nslice, slice_tok, cfg->split_best, cfg->split_tick, false,
+                                             reinterpret_cast<cudaStream_t>(stream)));
   int grid = std::min<long long>(B, static_cast<long long>(cfg->sel.blocks_per_sm) * cfg->nsm);
   return from_cuda(tg::launch_select(dev, a, false, grid, cfg->sel.smem, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -402,6 +406,10 @@ tg_status tg_verify(const void* target_logits, int32_t B, int32_t V, const int32
   cudaError_t e = cudaMemsetAsync(cfg->dev.tickets, 0, static_cast<size_t>(B) * sizeof(unsigned),
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return from_cuda(e);
+  int nslice = 0, slice_tok = 0;
+  if (split_plan(cfg, a.nrows, &nslice, &slice_tok))
+    return from_cuda(tg::launch_split_greedy(cfg->dev, a, nslice, slice_tok, cfg->split_best, cfg->split_tick, true,
+                                             reinterpret_cast<cudaStream_t>(stream)));
   int grid = std::min<long long>(a.nrows, static_cast<long long>(cfg->ver.blocks_per_sm) * cfg->nsm);
   return from_cuda(tg::launch_select(cfg->dev, a, true, grid, cfg->ver.smem, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -125,9 +125,11 @@ cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int gr
 // Greedy ids of rows [a.row_begin, a.nrows), each split over nslice CTAs of
 // slice_tok tokens (a multiple of 8); best and tick: one key and one count per
 // row, zero before the launch and left at zero after it (tg_kernels.cu).
+// verify: the rows are a plain verify's positions (no processors), and the
+// last position of each sequence writes its match (c.tickets zero before).
 int split_greedy_smem(int nwords);
 cudaError_t launch_split_greedy(const DevCfg& c, const SelArgs& a, int nslice, int slice_tok, unsigned long long* best,
-                                unsigned* tick, cudaStream_t s);
+                                unsigned* tick, bool verify, cudaStream_t s);
 cudaError_t launch_process(const DevCfg& c, const SelArgs& a, float* scores, unsigned* banbits, float* probs,
                            int smem, cudaStream_t s, const int32_t* st_ids = nullptr, const float* st_vals = nullptr);
 cudaError_t launch_state(const DevCfg& c, const SelArgs& a, int grid, int smem, cudaStream_t s,

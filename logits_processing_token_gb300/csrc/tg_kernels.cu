@@ -1106,7 +1106,8 @@ __device__ __forceinline__ unsigned order_key(float v) {
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
-    split_greedy_kernel(const DevCfg c, const SelArgs a, int slice_tok, unsigned long long* best, unsigned* tick) {
+    split_greedy_kernel(const DevCfg c, const SelArgs a, int slice_tok, unsigned long long* best, unsigned* tick,
+                        int verify) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SplitSmem& ss = *reinterpret_cast<SplitSmem*>(smem_raw);
   int* stage = reinterpret_cast<int*>(smem_raw + split_stage_off());
@@ -1121,8 +1122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The logits and histories may come from the kernel before this one.
   grid_dependency_wait();
   grid_dependents_launch();
-  const RowMeta rm = row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
-  if (rm.bad || rm.L == 0 || rm.forced) {
+  // verify (no processors): every position is read
+  const RowMeta rm = verify ? RowMeta{} : row_meta(c, a.hist, a.off, a.plen, row, a.nrows_total);
+  if (!verify && (rm.bad || rm.L == 0 || rm.forced)) {
     // not read: the first slice writes the row's id
     if (blockIdx.x == 0 && tid == 0) {
       if (rm.bad || rm.L == 0) {
@@ -1135,8 +1137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
-  const bool bitmaps = c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
-                       (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0));
+  const bool bitmaps = !verify && (c.rho != 1.0f || c.ngram > 0 || c.n_ban > 0 || c.n_bsup > 0 || c.n_seq > 0 ||
+                                    (c.n_eos > 0 && (c.min_length > 0 || c.min_new > 0)));
   if (bitmaps) build_row_bitmaps(c, a.hist, rm, M, N, a.nwords, stage, kSplitStage);   // M = history | banned
 
   const int t0 = static_cast<int>(blockIdx.x) * slice_tok;
@@ -1204,13 +1206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned long long k = atomicExch(best + row, 0ull);
       tick[row] = 0u;
       a.out[row] = static_cast<int>(~static_cast<unsigned>(k & 0xffffffffull));
+      if (verify) verify_ticket(c, a, row);   // the last position of a sequence writes its match
     }
   }
 }
 
 template <int DT>
 static cudaError_t launch_split_t(const DevCfg& c, const SelArgs& a, int nslice, int slice_tok,
-                                  unsigned long long* best, unsigned* tick, cudaStream_t s) {
+                                  unsigned long long* best, unsigned* tick, bool verify, cudaStream_t s) {
   auto k = split_greedy_kernel<DT>;
   const int smem = split_smem(a.nwords);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1225,7 +1228,7 @@ static cudaError_t launch_split_t(const DevCfg& c, const SelArgs& a, int nslice,
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k, c, a, slice_tok, best, tick);
+  e = cudaLaunchKernelEx(&cfg, k, c, a, slice_tok, best, tick, verify ? 1 : 0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1273,11 +1276,11 @@ static cudaError_t launch_sel_v(const DevCfg& c, const SelArgs& a, bool verify, 
 int split_greedy_smem(int nwords) { return split_smem(nwords); }
 
 cudaError_t launch_split_greedy(const DevCfg& c, const SelArgs& a, int nslice, int slice_tok, unsigned long long* best,
-                                unsigned* tick, cudaStream_t s) {
+                                unsigned* tick, bool verify, cudaStream_t s) {
   if (nslice < 1 || slice_tok < 8 || slice_tok % 8 != 0 || a.nrows <= a.row_begin || a.nrows - a.row_begin > 65535)
     return cudaErrorInvalidValue;
-  return c.dtype == kF32 ? launch_split_t<kF32>(c, a, nslice, slice_tok, best, tick, s)
-                         : launch_split_t<kBF16>(c, a, nslice, slice_tok, best, tick, s);
+  return c.dtype == kF32 ? launch_split_t<kF32>(c, a, nslice, slice_tok, best, tick, verify, s)
+                         : launch_split_t<kBF16>(c, a, nslice, slice_tok, best, tick, verify, s);
 }
 
 cudaError_t launch_select(const DevCfg& c, const SelArgs& a, bool verify, int grid, int smem, cudaStream_t s) {

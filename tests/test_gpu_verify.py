@@ -136,3 +136,36 @@ def test_verify_history_parity(mode, K):
         checked += 1
     assert checked >= B - 3
     assert om[3] == 0 and list(on[3]) == [-1] * (K + 1)
+
+
+@pytest.mark.parametrize("B,K", [(1, 1), (1, 5), (2, 2), (1, 8), (2, 5)])
+def test_verify_greedy_split_rows(B, K):
+    # Greedy verify of a batch this small splits each position's row over
+    # several CTAs (all but B=2, K=5: 12 positions of 13 slices do not fit one
+    # wave); the same sequences repeated into a batch of 64 (the config's
+    # max_batch) take one CTA per row.  Both, and a second call on the same
+    # config, give the same results.
+    import torch
+    import logits_processing_token_gb300 as tg
+    w, tgt, cand, p = make_case(B, K, "greedy")
+    om, on, cfg = run_gpu(w, tgt, cand, K)
+    t = torch.from_numpy(np.ascontiguousarray(tgt)).cuda()
+    c = torch.from_numpy(cand).cuda()
+    u = torch.from_numpy(np.ascontiguousarray(w.uniforms)).cuda()
+    om2 = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    on2 = torch.full((B, K + 1), -9, dtype=torch.int32, device="cuda")
+    tg.tg_verify(t, c, K, cfg, u, om2, on2)
+    torch.cuda.synchronize()
+    assert np.array_equal(om2.cpu().numpy(), om) and np.array_equal(on2.cpu().numpy(), on)
+    reps = 64 // B
+    tb = torch.from_numpy(np.ascontiguousarray(np.tile(tgt, (reps, 1, 1)))).cuda()
+    cb = torch.from_numpy(np.ascontiguousarray(np.tile(cand, (reps, 1)))).cuda()
+    ub = torch.from_numpy(np.ascontiguousarray(np.tile(w.uniforms, (reps, 1)))).cuda()
+    omb = torch.full((B * reps,), -9, dtype=torch.int32, device="cuda")
+    onb = torch.full((B * reps, K + 1), -9, dtype=torch.int32, device="cuda")
+    tg.tg_verify(tb, cb, K, cfg, ub, omb, onb)
+    torch.cuda.synchronize()
+    assert np.array_equal(omb.cpu().numpy()[:B], om) and np.array_equal(onb.cpu().numpy()[:B], on)
+    m_ref, n_ref, _ = O.verify(tgt, cand, K, p, w.uniforms)
+    assert list(om) == [int(x) for x in m_ref]
+    assert [list(r) for r in on] == [[int(x) for x in r] for r in n_ref]
