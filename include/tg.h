@@ -27,8 +27,9 @@
  *    fault: the kernel skips them and raises a bit in the config's status
  *    word (tg_query_status).
  *  - Calls that share a tg_config use its small device workspace (verify
- *    tickets, status word); issue them in stream order (one stream, or
- *    events between streams).  Use one config per concurrent stream.
+ *    tickets, the per-row keys and counts of split greedy rows, status
+ *    word); issue them in stream order (one stream, or events between
+ *    streams).  Use one config per concurrent stream.
  *  - Scores: the filter value F is -FLT_MAX; no score goes below it.
  */
 #ifndef TG_H_
@@ -193,6 +194,9 @@ const tg_config* tg_config_selection(const tg_config* cfg);
  * begin_suppress_tokens; then greedy argmax (lowest index among equal
  * maxima), or temperature, top_k, top_p and an inverse-CDF draw with
  * uniforms[b] over the kept tokens ordered by (score desc, index asc).
+ * A greedy batch small enough that its rows, cut into slices of about 16 KB
+ * of logits, fit one wave of CTAs is read with each row split over several
+ * CTAs (same ids; B <= max_batch); plain greedy tg_verify likewise.
  */
 tg_status tg_select(const void* logits, int32_t B, int32_t V, const int32_t* hist_ids,
                     const int64_t* hist_offsets, const int32_t* prompt_lens,
